@@ -1,0 +1,376 @@
+#!/usr/bin/env python
+"""Benchmark of the KPool-DSA forward on one GB300 per process.
+
+A step is one pass of the whole path over the T=32768 single-document
+workload: kpool_build (PoolLayout + pooling), dsa_index (Hadamard/FP8, FP8
+pool scoring, top-512 select + rows) and sparse_mla_fwd (64-head sparse
+latent attention).  Inputs are resident in HBM before the timed region; L2 is
+flushed (512 MB write) before every step, outside the step's CUDA events.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun every rank runs an independent replica (the path shards by
+documents / query rows with no exchange; one GPU per process).  Rank 0
+prints one JSON line.  ``--impl reference`` times the CPU oracle on the host
+cores instead (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KPool-DSA fwd tokens/s at 32K; indexer FP8 TFLOP/s; sparse MLA % of roofline"
+LAUNCHES_PER_STEP = 9   # layout scan, layout fill, pool, prep, quant q, quant k, score, select, sparse MLA
+
+
+def _args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=3, help="workload index (3 = T=32768 headline)")
+    ap.add_argument("--cpu-rows", type=int, default=96, help="query rows in the CPU-oracle sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16": float(d["bf16_tflops"]),
+                "bf16_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "source": "fallback"}
+
+
+def _work(wl):
+    """Algorithmic work of one step (closed forms over the documents)."""
+    pairs = 0
+    valid = 0
+    for L in wl.doc_lens:
+        for r in range(L):
+            n = (r + 1) // 4
+            pairs += n if n > wl.topk else 0
+            valid += 4 * min(wl.topk, n) + (r + 1) % 4
+    all_pairs = sum((r + 1) // 4 for L in wl.doc_lens for r in range(L))
+    return {
+        "score_flops": 2.0 * wl.n_idx_heads * wl.d_idx * all_pairs,
+        "score_pairs": all_pairs,
+        "scored_pairs": pairs,
+        "mla_flops": 2.0 * wl.n_heads * (2 * wl.d_lat) * valid,
+        "valid_slots": valid,
+        "mla_hbm_bytes": wl.T * wl.n_heads * wl.d_lat * 2 * 2 + wl.T * wl.d_lat * 2 + wl.T * wl.W * 4
+                         + wl.T * wl.n_heads * 4,
+    }
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.proc = None
+        self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                                          "-lms", "100"], stdout=self.tmp, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.tmp.flush()
+        rows = []
+        with open(self.tmp.name) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                rows.append(parts)
+        os.unlink(self.tmp.name)
+        if self.uuid:
+            mine = [r for r in rows if r[0] == self.uuid]
+            rows = mine or rows
+        uu = sorted({r[0] for r in rows})
+        if len(uu) > 1:
+            vis = os.environ.get("CUDA_VISIBLE_DEVICES", "0").split(",")[0]
+            rows = [r for r in rows if r[0] == uu[int(vis)]] if vis.isdigit() and int(vis) < len(uu) else rows
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4) if r[5 + k].lower().startswith("active")})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def _uuid():
+    try:
+        import torch
+        u = torch.cuda.get_device_properties(torch.cuda.current_device()).uuid
+        return "GPU-" + str(u)
+    except Exception:
+        return None
+
+
+# ----------------------------------------------------------------- CPU oracle sample
+
+def cpu_oracle_sample(wl, n_rows: int, seed: int = 0, inp=None):
+    """Times the CPU oracle on a bounded sample of the workload: the shared
+    per-forward work (layout, pooling, key quantisation) in full and the
+    per-query work (query quantisation, scores, select, rows, attention) on
+    n_rows seeded rows, extrapolated to all T rows."""
+    from oracle import kpool_oracle as O
+    from pooled_key_dsa_gb300 import workloads
+
+    inp = workloads.indexer_inputs(wl) if inp is None else inp
+    rows = np.sort(np.random.default_rng(seed).choice(wl.T, size=min(n_rows, wl.T), replace=False))
+    ql = workloads.q_lat(wl, rows=rows).float().numpy()
+    kf, qf, kvf = inp.k.float().numpy(), inp.q_idx.float().numpy(), inp.kv_lat.float().numpy()
+    t0 = time.perf_counter()
+    lay = O.pool_layout(wl.cu_seqlens)
+    kp = O.pool_keys(kf, inp.gate, inp.ape, lay)
+    k8, s_k = O.quantize_keys(kp)
+    t1 = time.perf_counter()
+    q8, s_q = O.quantize_queries(qf[rows])
+    S = O.scores_fp8(q8, s_q, k8, s_k, inp.w, lay, rows)
+    idx = np.stack([O.index_row(lay, int(i), O.select_pools(S[n], wl.topk), wl.W) for n, i in enumerate(rows)])
+    O.sparse_attention(ql, kvf, idx, wl.scale, rows)
+    t2 = time.perf_counter()
+    t_step = (t1 - t0) + (t2 - t1) * wl.T / len(rows)
+    return {"tokens_per_s": wl.T / t_step, "t_shared_s": t1 - t0, "t_rows_s": t2 - t1, "rows": len(rows),
+            "wall_s": t2 - t0}
+
+
+def run_reference(a):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from pooled_key_dsa_gb300 import workloads
+    wl = workloads.workload(a.config)
+    rows = max(8, a.cpu_rows // 3)
+    inp = workloads.indexer_inputs(wl)
+    vals, walls = [], []
+    for s in range(a.warmup + a.steps):
+        r = cpu_oracle_sample(wl, rows, seed=s, inp=inp)
+        if s >= a.warmup:
+            vals.append(r["tokens_per_s"])
+            walls.append(r["wall_s"])
+    v = statistics.median(vals)
+    cores = os.cpu_count()
+    sample = (f"per step: layout+pooling+key FP8 over all {wl.T} tokens, then {rows} seeded query rows "
+              f"(query FP8, scores, select, rows, attention) extrapolated to {wl.T} rows")
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": a.gpus,
+            "steps": a.steps, "warmup": a.warmup, "ms_per_step": 1e3 * wl.T / v, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": _config(wl),
+            "cpu_baseline": {"value": v, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+
+
+def _config(wl):
+    return {"workload": f"{wl.name}: packed THD, docs {list(wl.doc_lens)[:8]}{'...' if len(wl.doc_lens) > 8 else ''}",
+            "T": wl.T, "n_docs": len(wl.doc_lens), "H_i": wl.n_idx_heads, "d_i": wl.d_idx, "topk_pools": wl.topk,
+            "kpool": wl.kpool, "H": wl.n_heads, "D": wl.d_lat, "W": wl.W,
+            "l2": "flushed before every step (512 MB write, outside the step events)",
+            "parallelism": "replicas (one independent forward per GPU)"}
+
+
+# ----------------------------------------------------------------- our arm
+
+def main():
+    a = _args()
+    if a.impl == "reference":
+        run_reference(a)
+        return
+    import torch
+    import torch.distributed as dist
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    from pooled_key_dsa_gb300 import build as B
+    if rank == 0:
+        B.build()
+    if world > 1:
+        dist.barrier()
+    from pooled_key_dsa_gb300 import kpooldsa as K
+    from pooled_key_dsa_gb300 import workloads
+    K.lib()
+
+    wl = workloads.workload(a.config)
+    inp = workloads.all_inputs(wl)
+    dev = torch.device("cuda", local)
+    p = K.make_params(topk=wl.topk, n_idx_heads=wl.n_idx_heads, d_idx=wl.d_idx, n_heads=wl.n_heads,
+                      d_lat=wl.d_lat, scale=wl.scale)
+    T, W = wl.T, wl.W
+
+    host = {"cu_seqlens": torch.from_numpy(inp.cu_seqlens), "q_idx": inp.q_idx, "k": inp.k,
+            "gate": torch.from_numpy(inp.gate), "ape": torch.from_numpy(inp.ape), "w": torch.from_numpy(inp.w),
+            "q_lat": inp.q_lat, "kv_lat": inp.kv_lat}
+    d = {k: v.to(dev) for k, v in host.items()}
+    layout = K.PoolLayout(d["cu_seqlens"], T)
+    kpool = torch.empty((max(T // 4, 1), wl.d_idx), dtype=torch.float32, device=dev)
+    wsb = torch.empty(K.workspace_bytes(p, T, layout.n_docs), dtype=torch.uint8, device=dev)
+    idx = torch.empty((T, W), dtype=torch.int32, device=dev)
+    out = torch.empty_like(d["q_lat"])
+    lse = torch.empty((T, wl.n_heads), dtype=torch.float32, device=dev)
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(src, lay):
+        K.kpool_build(src["k"], src["gate"], src["ape"], src["cu_seqlens"], p, kpool_out=kpool, layout=lay)
+        K.dsa_index(src["q_idx"], src["w"], kpool, lay, wl.topk, p, workspace=wsb, indices=idx, W=W)
+        K.sparse_mla_fwd(src["q_lat"], src["kv_lat"], idx, wl.scale, out=out, lse=lse, status=lay.status)
+
+    for _ in range(a.warmup):
+        flush.zero_()
+        step(d, layout)
+    torch.cuda.synchronize()
+    st = K.check_status(layout.status)
+    if st != 0:
+        raise RuntimeError(f"device status {st}: {K.strerror(st)}")
+
+    # ---- device-timed steps (inputs resident)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(8)] for _ in range(a.steps)]
+    clocks = ClockSampler(_uuid())
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    wall0 = time.perf_counter()
+    for s in range(a.steps):
+        e = ev[s]
+        flush.zero_()
+        K.set_stage_events(e[2:6])
+        e[0].record(stream)
+        K.kpool_build(d["k"], d["gate"], d["ape"], d["cu_seqlens"], p, kpool_out=kpool, layout=layout)
+        e[1].record(stream)
+        K.dsa_index(d["q_idx"], d["w"], kpool, layout, wl.topk, p, workspace=wsb, indices=idx, W=W)
+        e[6].record(stream)
+        K.sparse_mla_fwd(d["q_lat"], d["kv_lat"], idx, wl.scale, out=out, lse=lse, status=layout.status)
+        e[7].record(stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    K.set_stage_events(None)
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop()
+    step_ms = [e[0].elapsed_time(e[7]) for e in ev]
+    t = {
+        "kpool_build": statistics.mean(e[0].elapsed_time(e[1]) for e in ev),
+        "hadamard_fp8": statistics.mean(e[2].elapsed_time(e[3]) for e in ev),
+        "score": statistics.mean(e[3].elapsed_time(e[4]) for e in ev),
+        "select": statistics.mean(e[4].elapsed_time(e[5]) for e in ev),
+        "dsa_index": statistics.mean(e[1].elapsed_time(e[6]) for e in ev),
+        "sparse_mla": statistics.mean(e[6].elapsed_time(e[7]) for e in ev),
+    }
+    total_ms = sum(step_ms)
+    tmax = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(tmax, op=dist.ReduceOp.MAX)
+    total_ms = float(tmax.item())
+    value = world * T * a.steps / (total_ms / 1e3)
+
+    # ---- end to end through the public API with host buffers
+    pinned = {k: v.pin_memory() for k, v in host.items()}
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in pinned.values())
+    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+    e2e_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(a.steps)]
+    for s in range(-1, a.steps):
+        flush.zero_()
+        if s >= 0:
+            e2e_ev[s][0].record(stream)
+        for k in d:
+            d[k].copy_(pinned[k], non_blocking=True)
+        step(d, layout)
+        out_h.copy_(out, non_blocking=True)
+        lse_h.copy_(lse, non_blocking=True)
+        if s >= 0:
+            e2e_ev[s][1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = sum(x.elapsed_time(y) for x, y in e2e_ev)
+    tm = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        dist.all_reduce(tm, op=dist.ReduceOp.MAX)
+    e2e_value = world * T * a.steps / (float(tm.item()) / 1e3)
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+    work = _work(wl)
+    peaks = _peaks()
+    mla_tflops = work["mla_flops"] / (t["sparse_mla"] / 1e3) / 1e12
+    score_tflops = work["score_flops"] / (t["score"] / 1e3) / 1e12
+    fp8_peak = 2.0 * peaks["bf16_sustained"]
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": a.steps,
+        "warmup": a.warmup, "ms_per_step": total_ms / a.steps, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e4m3 indexer + bf16 attention (fp32 accumulate)",
+        "data": "synthetic (seeded N(0,1) inputs, bf16 q/k/kv)", "config": _config(wl),
+        "indexer_fp8_tflops": score_tflops,
+        "sparse_mla_roofline_frac": mla_tflops / peaks["bf16_sustained"],
+        "stage_ms": t,
+        "roofline": {"bound": "tensor", "kernel": "sparse_mla", "achieved": mla_tflops,
+                     "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
+                     "frac": mla_tflops / peaks["bf16_sustained"], "traffic": None,
+                     "peak_kind": f"bf16 sustained, {peaks['source']}",
+                     "algorithmic": f"2*H*2D*valid_slots = {work['mla_flops']:.4e} FLOP per launch"},
+        "indexer_roofline": {"bound": "tensor", "kernel": "score", "achieved": score_tflops, "peak": fp8_peak,
+                             "unit": "TFLOP/s", "frac": score_tflops / fp8_peak, "traffic": None,
+                             "peak_kind": "fp8 = 2 x bf16 sustained (nominal ratio)",
+                             "algorithmic": f"2*H_i*d_i*pairs = {work['score_flops']:.4e} FLOP per launch"},
+        "clocks": clk,
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": LAUNCHES_PER_STEP * a.steps,
+        "wall_s_timed": wall,
+    }
+    if world == 1 and not a.no_cpu_baseline:
+        c = cpu_oracle_sample(wl, a.cpu_rows, inp=inp)
+        line["cpu_baseline"] = {
+            "value": c["tokens_per_s"], "unit": "tokens/s", "cores": os.cpu_count(), "kind": "oracle",
+            "sample": (f"layout+pooling+key FP8 over all {wl.T} tokens ({c['t_shared_s']:.2f} s) + {c['rows']} "
+                       f"seeded query rows ({c['t_rows_s']:.2f} s), extrapolated to {wl.T} rows")}
+    print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

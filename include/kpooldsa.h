@@ -1,0 +1,201 @@
+/*
+ * kpooldsa.h -- C ABI of the KPool-DSA forward on one GB300 (sm_103a).
+ *
+ * The forward of a GLM-5.3-Flash pooled-key DeepSeek-Sparse-Attention layer
+ * in three calls, each asynchronous on the caller's CUDA stream:
+ *
+ *   kpool_build     indexer keys -> per-document pooled keys + PoolLayout
+ *   dsa_index       Hadamard + FP8 queries and pooled keys, FP8 pool scores,
+ *                   top-k pools per query, padded int32 index rows
+ *   sparse_mla_fwd  NoPE sparse latent attention over the index rows
+ *
+ * Sources (page title, section):
+ *   prime-rl PR "GLM-5.3-Flash text model", Summary: the k-pool indexer
+ *     (pools of 4 per document from the first token, per-channel
+ *     softmax(gate+ape)-weighted mean, Hadamard rotation in an fp32
+ *     butterfly, FP8 scoring, complete pools ending at or before the query,
+ *     top 512, own incomplete pool, rows padded to a multiple of 128,
+ *     PoolLayout built once per forward).
+ *   NeMo AutoModel PR "add GLM-5.3-Flash training support", Changelog and
+ *     "cuDNN sparse MLA parity and performance": K absorbed into the query,
+ *     attention over a shared 512-wide latent K/V, 64 heads,
+ *     index_topk=2048, index_kpool=4, 2051 raw sparse slots.
+ *   miles "GLM-5.3-Flash" recipe, section 1: NoPE MLA, kpool-compressed
+ *     lightning indexer.
+ *
+ * Conventions for every call:
+ *   - Pointers named d_* or documented "device" are device pointers owned by
+ *     the caller; the library allocates nothing and keeps no pointer after
+ *     the call returns.
+ *   - bf16 tensors are passed as `const void*` holding IEEE bfloat16.
+ *   - All tensors are dense row-major (C order) with the shapes stated.
+ *   - The return value is a kpool_status.  Host-side checks (null or
+ *     misaligned pointers, unsupported sizes) return an error before any
+ *     launch.  Checks that need device data (cu_seqlens, index values)
+ *     record the first error in the caller's device status word, which
+ *     kpool_check_status() reads; such a call still completes and leaves
+ *     safe values (empty layouts, -1 rows, skipped slots) behind.
+ *   - Every call only enqueues work; none synchronises the stream except
+ *     kpool_check_status().
+ */
+#ifndef KPOOLDSA_H
+#define KPOOLDSA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same object as cudaStream_t / CUstream; NULL is the legacy default stream. */
+typedef struct CUstream_st* kpool_stream_t;
+
+typedef enum {
+    KPOOL_OK = 0,
+    KPOOL_ERR_INVALID_ARG = 1,  /* null pointer, bad count, bad parameter   */
+    KPOOL_ERR_SHAPE = 2,        /* size outside what the kernels support     */
+    KPOOL_ERR_ALIGN = 3,        /* pointer not aligned as documented         */
+    KPOOL_ERR_LAYOUT = 4,       /* cu_seqlens not 0 = c0 <= c1 <= ... = T    */
+    KPOOL_ERR_INDEX_RANGE = 5,  /* index row entry outside [-1, T)           */
+    KPOOL_ERR_TIMEOUT = 6,      /* a bounded device wait expired             */
+    KPOOL_ERR_CUDA = 7,         /* a CUDA runtime call failed                */
+    KPOOL_ERR_WORKSPACE = 8     /* workspace null or too small               */
+} kpool_status;
+
+/* Layer parameters.  kpool must be 4 (index_kpool); d_idx is 64 or 128;
+ * n_idx_heads is 1..64; n_heads is 1..64; d_lat must be 512; topk >= 1. */
+typedef struct {
+    int32_t kpool;        /* tokens per pool (4)                          */
+    int32_t topk;         /* pools kept per query (512 = 2048 positions)  */
+    int32_t n_idx_heads;  /* H_i, indexer heads                           */
+    int32_t d_idx;        /* d_i, indexer head width                      */
+    int32_t n_heads;      /* H, attention heads                           */
+    int32_t d_lat;        /* D, latent width (K and V)                    */
+    float scale;          /* attention softmax scale (1/sqrt(512))        */
+} kpool_params;
+
+/* PoolLayout: per-document pool geometry of a packed (THD) row of T tokens
+ * in n_docs documents.  All buffers are caller-allocated device memory,
+ * filled by kpool_build and read by dsa_index.
+ *   cu_seqlens     int32 [n_docs+1]  input: document starts, 0 .. T
+ *   cu_pools       int32 [n_docs+1]  cu_pools[d+1] - cu_pools[d] = floor(L_d/4)
+ *   pool_tok_start int32 [max_pools] first token of each pool (0 past the end)
+ *   tok_doc        int32 [T]         document of each token (-1 if the layout
+ *                                    is invalid)
+ *   status         int32 [1]         device error word (0 = OK); the caller
+ *                                    zeroes it before first use.
+ * max_pools must be >= floor(T/4), which bounds the pool count of any split. */
+typedef struct {
+    int32_t n_docs;
+    int32_t T;
+    int32_t max_pools;
+    const int32_t* cu_seqlens;
+    int32_t* cu_pools;
+    int32_t* pool_tok_start;
+    int32_t* tok_doc;
+    int32_t* status;
+} kpool_layout;
+
+/* Byte offsets of the intermediate tensors inside the dsa_index workspace
+ * (all 256-byte aligned).  Reading them after dsa_index is allowed and is how
+ * the intermediate values are inspected:
+ *   q8        uint8 E4M3 [T, H_i, d_i]  rotated, quantised queries
+ *   ws        fp32 [T, H_i]             w[i,h] * s_q[i,h]
+ *   k8        uint8 E4M3 [floor(T/4), d_i]
+ *   s_k       fp32 [floor(T/4)]         per-pool scale amax/448
+ *   pair_base int64 [n_docs+1]          start of each document's scores
+ *   sched     int32 [n_docs+1]          first scoring tile of each document
+ *   scores    fp32, compact triangle:   query i of document d at in-document
+ *             position r = i - cu_seqlens[d] has n = floor((r+1)/4) candidate
+ *             pools; its scores start at pair_base[d] + G(r) with
+ *             G(r) = 2a(a-1) + a(b+1), r = 4a + b, and are in pool order.
+ *             Rows with n <= topk are not scored (every candidate is kept). */
+typedef struct {
+    size_t q8, ws, k8, s_k, pair_base, sched, scores, total;
+} kpool_ws_offsets;
+
+/* Workspace bytes dsa_index needs for T tokens in at most n_docs documents
+ * (sized for the worst split: one document of T tokens).  Returns 0 on bad
+ * parameters. */
+size_t kpool_workspace_bytes(const kpool_params* p, int32_t T, int32_t n_docs);
+int kpool_workspace_offsets(const kpool_params* p, int32_t T, int32_t n_docs, kpool_ws_offsets* out);
+
+/* kpool_build: PoolLayout from cu_seqlens, then pooled indexer keys.
+ *   k      bf16 [T, d_idx]   indexer keys              (8-byte aligned)
+ *   gate   fp32 [T, d_idx]   pooling gate logits       (16-byte aligned)
+ *   ape    fp32 [kpool, d_idx] per-offset bias, indexed by position in pool
+ *   kpool_out fp32 [max_pools, d_idx]: row p = sum_j softmax_j(gate+ape) k,
+ *             rows >= the pool count are zero.
+ *   layout  filled in place; layout->cu_seqlens must equal cu_seqlens.
+ * Source: prime-rl PR "GLM-5.3-Flash text model", Summary (k-pool
+ * compression; PoolLayout built once per forward). */
+int kpool_build(const void* k, const float* gate, const float* ape, const int32_t* cu_seqlens,
+                int32_t n_docs, int32_t T, const kpool_params* p, float* kpool_out,
+                kpool_layout* layout, kpool_stream_t stream);
+
+/* dsa_index: the k-pool indexer after pooling.
+ *   q_idx  bf16 [T, H_i, d_i] indexer queries           (8-byte aligned)
+ *   w      fp32 [T, H_i]      per-query head weights
+ *   kpool  fp32 [max_pools, d_i] from kpool_build (16-byte aligned)
+ *   topk   pools kept per query (overrides p->topk when > 0)
+ *   workspace  kpool_workspace_bytes(p, T, n_docs) bytes, 256-byte aligned
+ *   indices    int32 [T, W]: for query i, the positions of its top-k pools
+ *              (4 each) and of its own incomplete pool up to i, ascending,
+ *              then -1.  W >= 4*topk + 3 and a multiple of 4 (2176 for topk
+ *              512 keeps rows a multiple of 128); 16-byte aligned.
+ * Score of query i for pool p: s_k[p] * sum_h w[i,h] s_q[i,h] ReLU(q8[i,h].k8[p]);
+ * ties go to the lower pool index.
+ * Source: prime-rl PR "GLM-5.3-Flash text model", Summary. */
+int dsa_index(const void* q_idx, const float* w, const float* kpool, const kpool_layout* layout,
+              int32_t topk, const kpool_params* p, void* workspace, size_t workspace_bytes,
+              int32_t* indices, int32_t W, kpool_stream_t stream);
+
+/* sparse_mla_fwd: absorbed NoPE sparse latent attention.
+ *   q_lat  bf16 [T, H, 512]  queries with K absorbed     (16-byte aligned)
+ *   kv_lat bf16 [T, 512]     shared latent key = value   (16-byte aligned)
+ *   indices int32 [T, W]     positions; -1 entries are skipped anywhere in
+ *                            the row; entries outside [-1, T) are skipped and
+ *                            flagged KPOOL_ERR_INDEX_RANGE in *status.
+ *   out    bf16 [T, H, 512]  sum_j softmax_j(scale q.kv_j) kv_j (RNE to bf16)
+ *   lse    fp32 [T, H]       ln sum_j exp(scale q.kv_j); -inf (and out = 0)
+ *                            for a row with no valid slot.
+ *   status int32 [1] device error word (may be NULL: errors then go unreported).
+ * Source: NeMo AutoModel PR "add GLM-5.3-Flash training support", Changelog
+ * (attention over the shared 512-wide latent, V projection applied after). */
+int sparse_mla_fwd(const void* q_lat, const void* kv_lat, const int32_t* indices, int32_t W,
+                   int32_t T, int32_t n_heads, float scale, void* out, float* lse,
+                   int32_t* status, kpool_stream_t stream);
+
+/* Stage entry point: top-k select + row expansion alone, fed with scores in
+ * the workspace's compact layout (same rules as dsa_index's last step).
+ *   scores   fp32, compact triangle as described for kpool_ws_offsets
+ *   pair_base int64 [n_docs+1] as described there */
+int kpool_stage_select(const float* scores, const int64_t* pair_base, const kpool_layout* layout,
+                       int32_t topk, int32_t* indices, int32_t W, kpool_stream_t stream);
+
+/* Stage timing hook.  With n = 4 events registered, every later dsa_index
+ * call records events[0] before its first launch, events[1] after the
+ * Hadamard/FP8 kernels, events[2] after the scoring kernel and events[3]
+ * after the select kernel, all on its stream (cudaEventRecord only; nothing
+ * synchronises).  events = NULL or n = 0 switches the hook off.  The events
+ * are cudaEvent_t handles owned by the caller; the hook is process-wide and
+ * not thread-safe. */
+typedef struct CUevent_st* kpool_event_t;
+int kpool_set_stage_events(kpool_event_t* events, int32_t n);
+
+/* Synchronises `stream`, then returns the device status word's value (a
+ * kpool_status), or KPOOL_ERR_CUDA if the stream or copy failed. */
+int kpool_check_status(const int32_t* status, kpool_stream_t stream);
+
+/* Static, human-readable text of a kpool_status. */
+const char* kpool_strerror(int code);
+
+/* Library version string, e.g. "kpooldsa 0.1 sm_103a". */
+const char* kpool_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KPOOLDSA_H */

@@ -1,0 +1,43 @@
+// Internal launch entry points behind the C ABI (one per kernel family).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "kpooldsa.h"
+
+namespace kpool {
+
+// Workspace geometry shared by the host layer and the launchers.
+struct WsLayout {
+    size_t q8, ws, k8, s_k, pair_base, sched, scores, total;
+};
+WsLayout ws_layout(int T, int n_docs, int max_pools, int n_idx_heads, int d_idx);
+
+int launch_kpool_build(const void* k, const float* gate, const float* ape, const kpool_layout& L, int d_idx,
+                       float* kpool_out, cudaStream_t stream);
+
+// Hadamard rotation + per-vector E4M3 quantisation of n_vec vectors of width d.
+// in_bf16 selects the input type (bf16 queries or fp32 pooled keys).  If
+// n_valid_dev is non-null, vectors at or past *n_valid_dev get zero codes and
+// scale.  If w is non-null, ws_out[v] = w[v] * scale[v]; scales may be null.
+int launch_hadamard_fp8(const void* x, bool in_bf16, int64_t n_vec, int d, const int32_t* n_valid_dev,
+                        const float* w, uint8_t* codes, float* scales, float* ws_out, cudaStream_t stream);
+
+// Per-document score bases and scoring-tile schedule (one tiny kernel).
+int launch_index_prep(const kpool_layout& L, int topk, int64_t* pair_base, int32_t* sched, cudaStream_t stream);
+
+// FP8 pool scores into the compact triangle.
+int launch_score(const uint8_t* q8, const float* ws, const uint8_t* k8, const float* s_k, const kpool_layout& L,
+                 const int64_t* pair_base, const int32_t* sched, int topk, int n_idx_heads, int d_idx,
+                 float* scores, cudaStream_t stream);
+
+// Top-k select, expansion to positions, own tail, -1 padding.
+int launch_select(const float* scores, const int64_t* pair_base, const kpool_layout& L, int topk, int32_t* indices,
+                  int W, cudaStream_t stream);
+
+int launch_sparse_mla(const uint16_t* q_lat, const uint16_t* kv_lat, const int32_t* indices, int W, int T,
+                      int n_heads, float scale, uint16_t* out, float* lse, int32_t* status, cudaStream_t stream);
+
+}  // namespace kpool

@@ -1,0 +1,206 @@
+// Per-query top-k pool select, expansion to token positions, own tail, -1 pad.
+//
+// prime-rl PR "GLM-5.3-Flash text model", Summary: a query keeps the top 512
+// of the complete pools that end at or before it and also attends to its own
+// incomplete pool; index rows are padded to a multiple of 128.  NeMo AutoModel
+// PR "add GLM-5.3-Flash training support": 2048 + 3 = 2051 raw slots.
+//
+// One 256-thread block per query row.  Scores become order-preserving uint32
+// keys; a three-level radix select (bits 31..20, 19..8, 7..0) finds the key K
+// of the topk-th best pool and how many pools equal to K still fit
+// (`need_eq`).  Level 1 histograms every key; the pools in the chosen level-1
+// bin are copied to a shared candidate list that levels 2 and 3 refine (if the
+// list overflows, those levels re-read the row).  A final ordered pass keeps
+// the pools with key > K plus the first `need_eq` pools with key == K (lower
+// pool index wins ties) and writes their positions in pool order, so the row
+// comes out ascending without a sort.
+#include <cstdint>
+
+#include "kpool_common.cuh"
+#include "kpool_launch.h"
+
+namespace kpool {
+
+namespace {
+
+constexpr int SEL_THREADS = 256;
+constexpr int SEL_WARPS = SEL_THREADS / 32;
+constexpr int HIST_BINS = 4096;
+constexpr int CAND_CAP = 4096;
+
+struct SelectSmem {
+    uint32_t hist[HIST_BINS];
+    uint32_t cand_key[CAND_CAP];
+    int32_t warp_tot[SEL_WARPS];
+    uint32_t n_cand;
+    uint32_t digit;
+    uint32_t remaining;
+};
+
+// Exclusive block scan of v (all threads); returns the exclusive prefix and
+// writes the block total.
+__device__ __forceinline__ int block_excl_scan(int v, int32_t* warp_tot, int& total) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) warp_tot[wid] = x;
+    __syncthreads();
+    int before = 0;
+    total = 0;
+#pragma unroll
+    for (int w = 0; w < SEL_WARPS; ++w) {
+        const int t = warp_tot[w];
+        before += (w < wid) ? t : 0;
+        total += t;
+    }
+    __syncthreads();
+    return before + x - v;
+}
+
+// Finds, in hist[0..nbins), the bin b where the count of keys in bins above b
+// is < remaining <= that count + hist[b]; stores b in s.digit and the updated
+// remaining (remaining - count above b) in s.remaining.
+__device__ void pick_digit(SelectSmem& s, int nbins, uint32_t remaining) {
+    const int per = nbins / SEL_THREADS;            // bins per thread (contiguous, descending order)
+    const int t = threadIdx.x;
+    // thread t owns bins [nbins - (t+1)*per, nbins - t*per), scanned from the top
+    int local = 0;
+    for (int j = 0; j < per; ++j) local += (int)s.hist[nbins - 1 - (t * per + j)];
+    int total;
+    const int above = block_excl_scan(local, s.warp_tot, total);
+    if ((uint32_t)above < remaining && remaining <= (uint32_t)(above + local)) {
+        uint32_t acc = (uint32_t)above;
+        for (int j = 0; j < per; ++j) {
+            const int b = nbins - 1 - (t * per + j);
+            const uint32_t h = s.hist[b];
+            if (acc < remaining && remaining <= acc + h) {
+                s.digit = (uint32_t)b;
+                s.remaining = remaining - acc;
+                break;
+            }
+            acc += h;
+        }
+    }
+    __syncthreads();
+}
+
+}  // namespace
+
+__global__ void __launch_bounds__(SEL_THREADS) select_kernel(const float* __restrict__ scores,
+                                                             const int64_t* __restrict__ pair_base,
+                                                             const int32_t* __restrict__ cu_seqlens,
+                                                             const int32_t* __restrict__ cu_pools,
+                                                             const int32_t* __restrict__ tok_doc, int n_docs, int T,
+                                                             int topk, int32_t* __restrict__ indices, int W) {
+    __shared__ SelectSmem s;
+    const int i = blockIdx.x;
+    const int t = threadIdx.x;
+    int32_t* row = indices + (int64_t)i * W;
+    const int d = (cu_pools[n_docs] < 0) ? -1 : tok_doc[i];
+    if (d < 0) {
+        for (int j = t; j < W; j += SEL_THREADS) row[j] = -1;
+        return;
+    }
+    const int s_d = cu_seqlens[d];
+    const int r = i - s_d;
+    const int n = (r + 1) / KPOOL;
+    const int tail = (r + 1) % KPOOL;
+    if (n <= topk) {                                  // every candidate is kept: the causal prefix
+        for (int j = t; j < W; j += SEL_THREADS) row[j] = (j <= r) ? s_d + j : -1;
+        return;
+    }
+    const float* sc = scores + pair_base[d] + pairs_before(r);
+
+    // ---- level 1: bits 31..20 over all keys
+    for (int b = t; b < HIST_BINS; b += SEL_THREADS) s.hist[b] = 0;
+    if (t == 0) s.n_cand = 0;
+    __syncthreads();
+    for (int p = t; p < n; p += SEL_THREADS) atomicAdd(&s.hist[score_key(sc[p]) >> 20], 1u);
+    __syncthreads();
+    pick_digit(s, HIST_BINS, (uint32_t)topk);
+    uint32_t prefix = s.digit << 20;
+    uint32_t remaining = s.remaining;
+    // candidates of the chosen bin
+    for (int p = t; p < n; p += SEL_THREADS) {
+        const uint32_t key = score_key(sc[p]);
+        if ((key >> 20) == (prefix >> 20)) {
+            const uint32_t slot = atomicAdd(&s.n_cand, 1u);
+            if (slot < CAND_CAP) s.cand_key[slot] = key;
+        }
+    }
+    __syncthreads();
+    const uint32_t nc = s.n_cand;
+    const bool from_list = nc <= CAND_CAP;
+
+    // ---- level 2: bits 19..8 among keys matching bits 31..20
+    for (int b = t; b < HIST_BINS; b += SEL_THREADS) s.hist[b] = 0;
+    __syncthreads();
+    if (from_list) {
+        for (uint32_t c = t; c < nc; c += SEL_THREADS) atomicAdd(&s.hist[(s.cand_key[c] >> 8) & 0xfffu], 1u);
+    } else {
+        for (int p = t; p < n; p += SEL_THREADS) {
+            const uint32_t key = score_key(sc[p]);
+            if ((key >> 20) == (prefix >> 20)) atomicAdd(&s.hist[(key >> 8) & 0xfffu], 1u);
+        }
+    }
+    __syncthreads();
+    pick_digit(s, HIST_BINS, remaining);
+    prefix |= s.digit << 8;
+    remaining = s.remaining;
+
+    // ---- level 3: bits 7..0 among keys matching bits 31..8
+    for (int b = t; b < 256; b += SEL_THREADS) s.hist[b] = 0;
+    __syncthreads();
+    if (from_list) {
+        for (uint32_t c = t; c < nc; c += SEL_THREADS) {
+            const uint32_t key = s.cand_key[c];
+            if ((key >> 8) == (prefix >> 8)) atomicAdd(&s.hist[key & 0xffu], 1u);
+        }
+    } else {
+        for (int p = t; p < n; p += SEL_THREADS) {
+            const uint32_t key = score_key(sc[p]);
+            if ((key >> 8) == (prefix >> 8)) atomicAdd(&s.hist[key & 0xffu], 1u);
+        }
+    }
+    __syncthreads();
+    pick_digit(s, 256, remaining);
+    const uint32_t K = prefix | s.digit;
+    const int need_eq = (int)s.remaining;
+
+    // ---- ordered compaction: positions of the kept pools, ascending
+    int sel_base = 0, eq_base = 0;
+    for (int c0 = 0; c0 < n; c0 += SEL_THREADS) {
+        const int p = c0 + t;
+        const uint32_t key = p < n ? score_key(sc[p]) : 0u;
+        const int gt = (p < n) && key > K;
+        const int eq = (p < n) && key == K;
+        int eq_tot, sel_tot;
+        const int eq_rank = eq_base + block_excl_scan(eq, s.warp_tot, eq_tot);
+        const int take = gt || (eq && eq_rank < need_eq);
+        const int slot = sel_base + block_excl_scan(take, s.warp_tot, sel_tot);
+        if (take && slot < topk) {
+            const int pos = s_d + KPOOL * p;
+            *reinterpret_cast<int4*>(row + KPOOL * slot) = make_int4(pos, pos + 1, pos + 2, pos + 3);
+        }
+        sel_base += sel_tot;
+        eq_base += eq_tot;
+    }
+    for (int j = KPOOL * topk + t; j < W; j += SEL_THREADS) {
+        const int q = j - KPOOL * topk;
+        row[j] = q < tail ? i - tail + 1 + q : -1;
+    }
+}
+
+int launch_select(const float* scores, const int64_t* pair_base, const kpool_layout& L, int topk, int32_t* indices,
+                  int W, cudaStream_t stream) {
+    if (L.T <= 0) return KPOOL_OK;
+    select_kernel<<<L.T, SEL_THREADS, 0, stream>>>(scores, pair_base, L.cu_seqlens, L.cu_pools, L.tok_doc, L.n_docs,
+                                                  L.T, topk, indices, W);
+    return cudaGetLastError() == cudaSuccess ? KPOOL_OK : KPOOL_ERR_CUDA;
+}
+
+}  // namespace kpool

@@ -1,0 +1,232 @@
+"""ctypes binding of ``libkpooldsa.so`` (C ABI in ``include/kpooldsa.h``).
+
+Argument marshalling only: every step of the forward runs in the library's
+CUDA kernels.  PyTorch supplies device memory and the current stream.  If the
+library has not been built, importing this module works but every call raises
+``KpoolUnavailable`` -- there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libkpooldsa.so")
+
+KPOOL_OK = 0
+ERRORS = {1: "KPOOL_ERR_INVALID_ARG", 2: "KPOOL_ERR_SHAPE", 3: "KPOOL_ERR_ALIGN", 4: "KPOOL_ERR_LAYOUT",
+          5: "KPOOL_ERR_INDEX_RANGE", 6: "KPOOL_ERR_TIMEOUT", 7: "KPOOL_ERR_CUDA", 8: "KPOOL_ERR_WORKSPACE"}
+CODES = {v: k for k, v in ERRORS.items()}
+
+EXPORTED = ("kpool_workspace_bytes", "kpool_workspace_offsets", "kpool_build", "dsa_index", "sparse_mla_fwd",
+            "kpool_stage_select", "kpool_set_stage_events", "kpool_check_status", "kpool_strerror", "kpool_version")
+
+
+class KpoolUnavailable(ImportError):
+    pass
+
+
+class KpoolError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {ERRORS.get(code, code)} ({strerror(code)})")
+
+
+class Params(ctypes.Structure):
+    _fields_ = [("kpool", ctypes.c_int32), ("topk", ctypes.c_int32), ("n_idx_heads", ctypes.c_int32),
+                ("d_idx", ctypes.c_int32), ("n_heads", ctypes.c_int32), ("d_lat", ctypes.c_int32),
+                ("scale", ctypes.c_float)]
+
+
+class LayoutC(ctypes.Structure):
+    _fields_ = [("n_docs", ctypes.c_int32), ("T", ctypes.c_int32), ("max_pools", ctypes.c_int32),
+                ("cu_seqlens", ctypes.c_void_p), ("cu_pools", ctypes.c_void_p),
+                ("pool_tok_start", ctypes.c_void_p), ("tok_doc", ctypes.c_void_p), ("status", ctypes.c_void_p)]
+
+
+class WsOffsets(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in ("q8", "ws", "k8", "s_k", "pair_base", "sched", "scores", "total")]
+
+
+_lib = None
+
+
+def lib():
+    """The loaded library (raises KpoolUnavailable when it is not built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_LIB_PATH):
+            raise KpoolUnavailable(f"{_LIB_PATH} is not built; run pooled_key_dsa_gb300.build.build()")
+        L = ctypes.CDLL(_LIB_PATH)
+        vp, i32, sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t
+        L.kpool_workspace_bytes.argtypes = [ctypes.POINTER(Params), i32, i32]
+        L.kpool_workspace_bytes.restype = sz
+        L.kpool_workspace_offsets.argtypes = [ctypes.POINTER(Params), i32, i32, ctypes.POINTER(WsOffsets)]
+        L.kpool_build.argtypes = [vp, vp, vp, vp, i32, i32, ctypes.POINTER(Params), vp, ctypes.POINTER(LayoutC), vp]
+        L.dsa_index.argtypes = [vp, vp, vp, ctypes.POINTER(LayoutC), i32, ctypes.POINTER(Params), vp, sz, vp, i32,
+                                vp]
+        L.sparse_mla_fwd.argtypes = [vp, vp, vp, i32, i32, i32, ctypes.c_float, vp, vp, vp, vp]
+        L.kpool_stage_select.argtypes = [vp, vp, ctypes.POINTER(LayoutC), i32, vp, i32, vp]
+        L.kpool_check_status.argtypes = [vp, vp]
+        L.kpool_set_stage_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), i32]
+        L.kpool_strerror.argtypes = [ctypes.c_int]
+        L.kpool_strerror.restype = ctypes.c_char_p
+        L.kpool_version.restype = ctypes.c_char_p
+        for name in ("kpool_workspace_offsets", "kpool_build", "dsa_index", "sparse_mla_fwd", "kpool_stage_select",
+                     "kpool_set_stage_events", "kpool_check_status"):
+            getattr(L, name).restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def strerror(code: int) -> str:
+    try:
+        return lib().kpool_strerror(int(code)).decode()
+    except KpoolUnavailable:
+        return "library not built"
+
+
+def _check(rc: int, what: str):
+    if rc != KPOOL_OK:
+        raise KpoolError(rc, what)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _want(t, dtype, shape, name):
+    if not isinstance(t, torch.Tensor) or t.device.type != "cuda":
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def make_params(topk=512, n_idx_heads=32, d_idx=128, n_heads=64, d_lat=512, scale=None, kpool=4) -> Params:
+    if scale is None:
+        scale = 1.0 / math.sqrt(d_lat)
+    return Params(kpool, topk, n_idx_heads, d_idx, n_heads, d_lat, scale)
+
+
+def row_width(topk: int, kpool: int = 4) -> int:
+    raw = kpool * topk + kpool - 1
+    return 128 * ((raw + 127) // 128)
+
+
+class PoolLayout:
+    """Device buffers of a PoolLayout plus the C struct that points at them."""
+
+    def __init__(self, cu_seqlens: torch.Tensor, T: int, status: torch.Tensor | None = None):
+        _want(cu_seqlens, torch.int32, None, "cu_seqlens")
+        dev = cu_seqlens.device
+        self.n_docs = cu_seqlens.numel() - 1
+        self.T = int(T)
+        self.max_pools = self.T // 4
+        self.cu_seqlens = cu_seqlens
+        self.cu_pools = torch.zeros(self.n_docs + 1, dtype=torch.int32, device=dev)
+        self.pool_tok_start = torch.zeros(max(self.max_pools, 1), dtype=torch.int32, device=dev)
+        self.tok_doc = torch.zeros(max(self.T, 1), dtype=torch.int32, device=dev)
+        self.status = status if status is not None else torch.zeros(1, dtype=torch.int32, device=dev)
+        self.c = LayoutC(self.n_docs, self.T, self.max_pools, cu_seqlens.data_ptr(), self.cu_pools.data_ptr(),
+                         self.pool_tok_start.data_ptr(), self.tok_doc.data_ptr(), self.status.data_ptr())
+
+
+def workspace_bytes(p: Params, T: int, n_docs: int) -> int:
+    return int(lib().kpool_workspace_bytes(ctypes.byref(p), T, n_docs))
+
+
+def workspace_offsets(p: Params, T: int, n_docs: int) -> WsOffsets:
+    o = WsOffsets()
+    _check(lib().kpool_workspace_offsets(ctypes.byref(p), T, n_docs, ctypes.byref(o)), "kpool_workspace_offsets")
+    return o
+
+
+def kpool_build(k, gate, ape, cu_seqlens, p: Params, kpool_out=None, layout: PoolLayout | None = None,
+                stream=None):
+    """Pooled keys fp32 [T//4, d_idx] and the PoolLayout (both on k's device)."""
+    T, d = k.shape
+    _want(k, torch.bfloat16, (T, p.d_idx), "k")
+    _want(gate, torch.float32, (T, p.d_idx), "gate")
+    _want(ape, torch.float32, (p.kpool, p.d_idx), "ape")
+    if layout is None:
+        layout = PoolLayout(cu_seqlens, T)
+    if kpool_out is None:
+        kpool_out = torch.empty((max(layout.max_pools, 1), p.d_idx), dtype=torch.float32, device=k.device)
+    _check(lib().kpool_build(_ptr(k), _ptr(gate), _ptr(ape), _ptr(cu_seqlens), layout.n_docs, T, ctypes.byref(p),
+                             _ptr(kpool_out), ctypes.byref(layout.c), _stream(stream)), "kpool_build")
+    return kpool_out, layout
+
+
+def dsa_index(q_idx, w, kpool, layout: PoolLayout, topk: int, p: Params, workspace=None, indices=None, W=None,
+              stream=None):
+    """int32 index rows [T, W] (W defaults to the multiple of 128 above 4*topk+3)."""
+    T = layout.T
+    _want(q_idx, torch.bfloat16, (T, p.n_idx_heads, p.d_idx), "q_idx")
+    _want(w, torch.float32, (T, p.n_idx_heads), "w")
+    _want(kpool, torch.float32, None, "kpool")
+    W = row_width(topk) if W is None else int(W)
+    nbytes = workspace_bytes(p, T, layout.n_docs)
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=q_idx.device)
+    if indices is None:
+        indices = torch.empty((T, W), dtype=torch.int32, device=q_idx.device)
+    _check(lib().dsa_index(_ptr(q_idx), _ptr(w), _ptr(kpool), ctypes.byref(layout.c), topk, ctypes.byref(p),
+                           _ptr(workspace), workspace.numel(), _ptr(indices), W, _stream(stream)), "dsa_index")
+    return indices
+
+
+def sparse_mla_fwd(q_lat, kv_lat, indices, scale: float, out=None, lse=None, status=None, stream=None):
+    """(out bf16 [T, H, 512], lse fp32 [T, H])."""
+    T, H, D = q_lat.shape
+    _want(q_lat, torch.bfloat16, (T, H, D), "q_lat")
+    _want(kv_lat, torch.bfloat16, (T, D), "kv_lat")
+    _want(indices, torch.int32, None, "indices")
+    if indices.dim() != 2 or indices.shape[0] != T:
+        raise ValueError("indices must be [T, W]")
+    if out is None:
+        out = torch.empty_like(q_lat)
+    if lse is None:
+        lse = torch.empty((T, H), dtype=torch.float32, device=q_lat.device)
+    _check(lib().sparse_mla_fwd(_ptr(q_lat), _ptr(kv_lat), _ptr(indices), indices.shape[1], T, H, float(scale),
+                                _ptr(out), _ptr(lse), _ptr(status), _stream(stream)), "sparse_mla_fwd")
+    return out, lse
+
+
+def stage_select(scores, pair_base, layout: PoolLayout, topk: int, W=None, indices=None, stream=None):
+    W = row_width(topk) if W is None else int(W)
+    if indices is None:
+        indices = torch.empty((layout.T, W), dtype=torch.int32, device=scores.device)
+    _check(lib().kpool_stage_select(_ptr(scores), _ptr(pair_base), ctypes.byref(layout.c), topk, _ptr(indices), W,
+                                    _stream(stream)), "kpool_stage_select")
+    return indices
+
+
+def check_status(status, stream=None) -> int:
+    """Synchronises the stream and returns the device status word."""
+    return int(lib().kpool_check_status(_ptr(status), _stream(stream)))
+
+
+def set_stage_events(events) -> None:
+    """Register 4 torch.cuda.Event(enable_timing=True) objects (or None) for
+    the dsa_index stage timing hook."""
+    if not events:
+        _check(lib().kpool_set_stage_events(None, 0), "kpool_set_stage_events")
+        return
+    arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
+    _check(lib().kpool_set_stage_events(arr, len(events)), "kpool_set_stage_events")
+
+
+def version() -> str:
+    return lib().kpool_version().decode()

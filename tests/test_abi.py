@@ -1,0 +1,95 @@
+"""The C-ABI library builds for sm_103a, loads, and exports every function
+that include/kpooldsa.h declares; host-side argument checks answer without a
+GPU (no call here reaches a kernel)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from pooled_key_dsa_gb300 import build as B
+from pooled_key_dsa_gb300 import kpooldsa as K
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "kpooldsa.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    B.build()
+    return K.lib()
+
+
+def _declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w]*\s*\**\s+\**\s*([A-Za-z_]\w*)\s*\(", text, flags=re.M)
+    return sorted(set(n for n in names if n not in ("if", "while")))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared_functions()
+    assert {"kpool_build", "dsa_index", "sparse_mla_fwd"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) <= set(K.EXPORTED) | {n for n in names if hasattr(lib, n)}
+
+
+def test_version_and_strerror(lib):
+    assert "sm_103a" in K.version()
+    for code in range(0, 9):
+        assert K.strerror(code) != "unknown error"
+    assert K.strerror(99) == "unknown error"
+
+
+def _closed_pairs(T):
+    a, b = divmod(T, 4)
+    return 2 * a * (a - 1) + a * (b + 1)
+
+
+def test_workspace_geometry(lib):
+    p = K.make_params()
+    for T in (0, 1, 512, 4096, 32768):
+        o = K.workspace_offsets(p, T, 3)
+        assert o.q8 == 0 and o.total == K.workspace_bytes(p, T, 3)
+        for name in ("q8", "ws", "k8", "s_k", "pair_base", "sched", "scores", "total"):
+            assert getattr(o, name) % 256 == 0
+        assert o.ws >= T * 32 * 128 and o.scores - o.sched >= 4 * 4
+        assert o.total - o.scores >= 4 * _closed_pairs(T)
+    # the headline workload's score triangle: 134,209,536 pairs
+    assert _closed_pairs(32768) == 134209536
+    assert K.workspace_bytes(K.make_params(d_idx=96), 64, 1) == 0
+
+
+def test_host_checks_reject_bad_arguments(lib):
+    p = K.make_params()
+    bad = K.make_params(topk=0)
+    lay = K.LayoutC(1, 64, 16, 16, 16, 16, 16, 16)   # fake non-null device pointers
+    vp = ctypes.c_void_p
+    # invalid parameters
+    assert lib.kpool_build(vp(16), vp(16), vp(16), vp(16), 1, 64, ctypes.byref(bad), vp(16), ctypes.byref(lay),
+                           None) == K.CODES["KPOOL_ERR_INVALID_ARG"]
+    # layout / argument mismatch
+    assert lib.kpool_build(vp(16), vp(16), vp(16), vp(32), 1, 64, ctypes.byref(p), vp(16), ctypes.byref(lay),
+                           None) == K.CODES["KPOOL_ERR_INVALID_ARG"]
+    # misaligned gate
+    assert lib.kpool_build(vp(16), vp(20), vp(16), vp(16), 1, 64, ctypes.byref(p), vp(16), ctypes.byref(lay),
+                           None) == K.CODES["KPOOL_ERR_ALIGN"]
+    # row width too small for topk
+    assert lib.dsa_index(vp(16), vp(16), vp(16), ctypes.byref(lay), 512, ctypes.byref(p), vp(256), 1 << 30, vp(16),
+                         2048, None) == K.CODES["KPOOL_ERR_SHAPE"]
+    # workspace too small
+    assert lib.dsa_index(vp(16), vp(16), vp(16), ctypes.byref(lay), 8, ctypes.byref(p), vp(256), 10, vp(16), 128,
+                         None) == K.CODES["KPOOL_ERR_WORKSPACE"]
+    # attention: too many heads, bad alignment
+    assert lib.sparse_mla_fwd(vp(16), vp(16), vp(16), 128, 64, 65, 0.1, vp(16), vp(16), None,
+                              None) == K.CODES["KPOOL_ERR_SHAPE"]
+    assert lib.sparse_mla_fwd(vp(8), vp(16), vp(16), 128, 64, 64, 0.1, vp(16), vp(16), None,
+                              None) == K.CODES["KPOOL_ERR_ALIGN"]
+    assert lib.kpool_check_status(None, None) == K.CODES["KPOOL_ERR_INVALID_ARG"]
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(K, "_lib", None)
+    monkeypatch.setattr(K, "_LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(K.KpoolUnavailable):
+        K.lib()

@@ -1,0 +1,311 @@
+"""GPU-vs-oracle parity of every step of the KPool-DSA forward, through the C
+ABI, on the seeded workloads and edge cases."""
+import numpy as np
+import pytest
+import torch
+
+from oracle import kpool_oracle as O
+from pooled_key_dsa_gb300 import build as B
+from pooled_key_dsa_gb300 import kpooldsa as K
+from pooled_key_dsa_gb300 import workloads
+from tests import kpool_parity as KP
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    B.build()
+    assert torch.cuda.is_available(), "GPU tests need CUDA"
+    K.lib()
+
+
+def _check_layout(res, lay_o, wl):
+    assert res["status"] == 0
+    np.testing.assert_array_equal(res["cu_pools"], lay_o["cu_pools"])
+    np.testing.assert_array_equal(res["pool_tok_start"][:lay_o["n_pools"]], lay_o["pool_tok_start"])
+    np.testing.assert_array_equal(res["tok_doc"], lay_o["tok_doc"])
+
+
+def _check_kpool(res, inp, lay_o):
+    kp_o = O.pool_keys(inp.k.float().numpy(), inp.gate, inp.ape, lay_o)
+    P = lay_o["n_pools"]
+    kp_g = res["kpool"][:P]
+    kf = np.abs(inp.k.float().numpy())
+    mag = np.stack([kf[lay_o["pool_tok_start"] + j] for j in range(4)]).max(axis=0) if P else np.zeros((0, 1))
+    err = np.abs(kp_g.astype(np.float64) - kp_o.astype(np.float64))
+    assert np.all(err <= KP.KPOOL_RTOL * mag + 1e-30), float((err / np.maximum(mag, 1e-30)).max())
+    assert np.all(res["kpool"][P:] == 0)
+    return kp_o
+
+
+def _full_parity(idx, rows=None, attn_rows=None):
+    wl = workloads.workload(idx)
+    inp = workloads.indexer_inputs(wl)
+    dev = KP.to_dev(inp)
+    res = KP.run_indexer(wl, dev)
+    lay_o = O.pool_layout(wl.cu_seqlens)
+    _check_layout(res, lay_o, wl)
+    kp_o = _check_kpool(res, inp, lay_o)
+
+    # FP8 keys: the oracle's quantiser on the GPU's pooled keys is bit-exact,
+    # and so is the oracle's own end-to-end chain
+    k8_o, sk_o = O.quantize_keys(res["kpool"])
+    np.testing.assert_array_equal(res["k8"], k8_o)
+    np.testing.assert_array_equal(res["s_k"].view(np.uint32), sk_o.view(np.uint32))
+    k8_e2e, _ = O.quantize_keys(kp_o)
+    assert np.array_equal(res["k8"], k8_e2e)
+
+    rows = np.arange(wl.T) if rows is None else rows
+    qf = inp.q_idx.float().numpy()
+    q8_o, sq_o = O.quantize_queries(qf[rows])
+    np.testing.assert_array_equal(res["q8"][rows], q8_o)
+    ws_o = (inp.w[rows] * sq_o).astype(np.float32)
+    np.testing.assert_array_equal(res["ws"][rows].view(np.uint32), ws_o.view(np.uint32))
+
+    # scores of the scored rows (fp32 accumulation order differs from fp64)
+    S_o = O.scores_fp8(q8_o, sq_o, res["k8"], res["s_k"], inp.w, lay_o, rows)
+    worst = 0.0
+    for n, i in enumerate(rows):
+        g = KP.gpu_row_scores(res, lay_o, int(i))
+        if g is None:
+            continue
+        o = S_o[n].astype(np.float64)
+        scale = max(np.abs(o).max(), 1e-30)
+        worst = max(worst, float(np.abs(g - o).max() / scale))
+    assert worst <= 1e-5, worst
+
+    stats = KP.compare_rows(res["indices"][rows], lay_o, rows, S_o, wl.topk, res["W"])
+    print(f"\n[{wl.name}] index rows: {stats['exact']}/{stats['rows']} bit-exact, "
+          f"{stats['boundary_rows']} boundary rows ({stats['boundary_pools']} pools), hard {stats['hard']}; "
+          f"score rel err {worst:.2e}")
+    assert stats["hard"] == 0, stats["hard_rows"][:10]
+
+    # attention, evaluated by the oracle on the GPU's own index rows
+    attn_rows = rows if attn_rows is None else attn_rows
+    ql = workloads.q_lat(wl)
+    out, lse = K.sparse_mla_fwd(ql.cuda(), dev["kv_lat"], res["indices_dev"], wl.scale)
+    torch.cuda.synchronize()
+    out_g = out[torch.from_numpy(attn_rows).cuda()].float().cpu().numpy()
+    lse_g = lse[torch.from_numpy(attn_rows).cuda()].cpu().numpy()
+    out_o, lse_o = O.sparse_attention(ql[torch.from_numpy(attn_rows)].float().numpy(), inp.kv_lat.float().numpy(),
+                                      res["indices"][attn_rows], wl.scale, attn_rows)
+    mx, mean, le = KP.attention_check(out_g, lse_g, out_o, lse_o)
+    print(f"[{wl.name}] attention: max abs {mx:.3e}, mean abs {mean:.3e}, lse {le:.3e}")
+    assert mx <= KP.OUT_MAX_ABS and mean <= KP.OUT_MEAN_ABS and le <= KP.LSE_ABS
+    return wl, res
+
+
+def test_parity_tiny_workload():
+    _full_parity(0)
+
+
+def test_parity_single_doc_4096_cutover():
+    wl = workloads.workload(1)
+    _full_parity(1, rows=KP.sample_rows(wl, n_uniform=400, seed=1))
+
+
+def test_parity_packed_8192_six_docs():
+    wl = workloads.workload(2)
+    _full_parity(2, rows=KP.sample_rows(wl, n_uniform=400, seed=2))
+
+
+def test_parity_headline_32768():
+    wl = workloads.workload(3)
+    _full_parity(3, rows=KP.sample_rows(wl, n_uniform=256, seed=3))
+
+
+@pytest.mark.slow
+def test_parity_long_131072():
+    wl = workloads.workload(4)
+    _full_parity(4, rows=KP.sample_rows(wl, n_uniform=192, seed=4))
+
+
+# ----------------------------------------------------------------- stage isolation
+
+def _scores_buffer(wl, lay_o, topk, S_rows, rows):
+    """Oracle scores placed in the workspace's compact triangle layout."""
+    cu = wl.cu_seqlens
+    pair_base = np.zeros(len(cu), np.int64)
+    for d in range(len(cu) - 1):
+        L = int(cu[d + 1] - cu[d])
+        a, b = divmod(L, 4)
+        pair_base[d + 1] = pair_base[d] + 2 * a * (a - 1) + a * (b + 1)
+    buf = np.zeros(max(int(pair_base[-1]), 1), np.float32)
+    for n, i in enumerate(rows):
+        d, r, n_i, _ = O.query_geometry(lay_o, int(i))
+        a, b = divmod(r, 4)
+        s = int(pair_base[d]) + 2 * a * (a - 1) + a * (b + 1)
+        buf[s:s + n_i] = S_rows[n]
+    return buf, pair_base
+
+
+def _stage_select(wl, S_rows, topk):
+    lay_o = O.pool_layout(wl.cu_seqlens)
+    rows = np.arange(wl.T)
+    buf, pb = _scores_buffer(wl, lay_o, topk, S_rows, rows)
+    cu = torch.from_numpy(wl.cu_seqlens).cuda()
+    p = KP.params_of(wl)
+    k = torch.zeros((wl.T, wl.d_idx), dtype=torch.bfloat16, device="cuda")
+    gate = torch.zeros((wl.T, wl.d_idx), dtype=torch.float32, device="cuda")
+    ape = torch.zeros((4, wl.d_idx), dtype=torch.float32, device="cuda")
+    _, lay = K.kpool_build(k, gate, ape, cu, p)
+    W = K.row_width(topk)
+    idx = K.stage_select(torch.from_numpy(buf).cuda(), torch.from_numpy(pb).cuda(), lay, topk, W=W)
+    got = idx.cpu().numpy()
+    want = np.stack([O.index_row(lay_o, i, O.select_pools(S_rows[i], topk), W) for i in range(wl.T)])
+    return got, want
+
+
+def test_stage_select_bit_exact_on_oracle_scores():
+    wl = workloads.workload(1)
+    inp = workloads.indexer_inputs(wl)
+    r = O.indexer(inp.q_idx.float().numpy(), inp.k.float().numpy(), inp.gate, inp.ape, inp.w, wl.cu_seqlens,
+                  wl.topk, wl.W, with_scores=True)
+    got, want = _stage_select(wl, r["scores"], wl.topk)
+    np.testing.assert_array_equal(got, want)
+
+
+@pytest.mark.parametrize("kind", ["few_values", "zeros_signed", "all_equal", "negative"])
+def test_stage_select_ties(kind):
+    wl = workloads.custom("ties", 7, (1500, 1037, 3), topk=64)
+    lay_o = O.pool_layout(wl.cu_seqlens)
+    rng = np.random.default_rng({"few_values": 1, "zeros_signed": 2, "all_equal": 3, "negative": 4}[kind])
+    S = []
+    for i in range(wl.T):
+        n = O.query_geometry(lay_o, i)[2]
+        if kind == "few_values":
+            s = rng.integers(-2, 3, n).astype(np.float32) * np.float32(0.25)
+        elif kind == "zeros_signed":
+            s = np.where(rng.random(n) < 0.5, np.float32(-0.0), np.float32(0.0)).astype(np.float32)
+            s[rng.random(n) < 0.05] = 1.0
+        elif kind == "all_equal":
+            s = np.full(n, 3.5, np.float32)
+        else:
+            s = -np.abs(rng.standard_normal(n)).astype(np.float32)
+        S.append(s)
+    got, want = _stage_select(wl, S, wl.topk)
+    np.testing.assert_array_equal(got, want)
+
+
+# ----------------------------------------------------------------- edge cases
+
+@pytest.mark.parametrize("lens", [(1,), (3,), (4,), (5, 0, 7), (2, 1, 3, 2), (130, 0, 0, 257), (4096 + 3,)])
+def test_edge_layouts_and_rows(lens):
+    wl = workloads.custom("edge", 11, lens, n_idx_heads=4, d_idx=64, topk=8, n_heads=4)
+    inp = workloads.indexer_inputs(wl)
+    dev = KP.to_dev(inp)
+    res = KP.run_indexer(wl, dev)
+    lay_o = O.pool_layout(wl.cu_seqlens)
+    _check_layout(res, lay_o, wl)
+    _check_kpool(res, inp, lay_o)
+    rows = np.arange(wl.T)
+    r = O.indexer(inp.q_idx.float().numpy(), inp.k.float().numpy(), inp.gate, inp.ape, inp.w, wl.cu_seqlens,
+                  wl.topk, wl.W, with_scores=True)
+    stats = KP.compare_rows(res["indices"], lay_o, rows, r["scores"], wl.topk, res["W"])
+    assert stats["hard"] == 0
+
+
+def test_invalid_cu_seqlens_sets_status_and_empty_rows():
+    wl = workloads.custom("bad", 3, (40, 24), n_idx_heads=4, d_idx=64, topk=8, n_heads=4)
+    inp = workloads.indexer_inputs(wl)
+    dev = KP.to_dev(inp)
+    dev["cu_seqlens"] = torch.tensor([0, 50, 40], dtype=torch.int32, device="cuda")   # decreasing, wrong end
+    res = KP.run_indexer(wl, dev)
+    assert res["status"] == K.CODES["KPOOL_ERR_LAYOUT"]
+    assert res["cu_pools"][-1] == -1
+    assert np.all(res["indices"] == -1)
+    assert np.all(res["kpool"] == 0)
+
+
+def test_sparse_mla_index_range_and_empty_rows():
+    wl = workloads.custom("mla_edge", 5, (300,), n_heads=64)
+    inp = workloads.indexer_inputs(wl)
+    ql = workloads.q_lat(wl)
+    T, W = wl.T, 256
+    rng = np.random.default_rng(0)
+    idx = np.full((T, W), -1, np.int32)
+    for i in range(T):
+        n = min(i + 1, int(rng.integers(0, 200)))
+        idx[i, :n] = np.sort(rng.choice(T, n, replace=False))
+    idx[5, 3] = T + 7            # out of range: skipped and flagged
+    idx[6, 0] = -5
+    idx[7, :] = -1               # empty row
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, lse = K.sparse_mla_fwd(ql.cuda(), inp.kv_lat.cuda(), torch.from_numpy(idx).cuda(), wl.scale, status=st)
+    assert K.check_status(st) == K.CODES["KPOOL_ERR_INDEX_RANGE"]
+    ref_idx = idx.copy()
+    ref_idx[(ref_idx < -1) | (ref_idx >= T)] = -1
+    rows = np.arange(T)
+    out_o, lse_o = O.sparse_attention(ql.float().numpy(), inp.kv_lat.float().numpy(), ref_idx, wl.scale, rows)
+    out_g, lse_g = out.float().cpu().numpy(), lse.cpu().numpy()
+    assert np.all(out_g[7] == 0) and np.all(np.isneginf(lse_g[7]))
+    mx, mean, le = KP.attention_check(out_g, lse_g, out_o, lse_o)
+    assert mx <= KP.OUT_MAX_ABS and mean <= KP.OUT_MEAN_ABS and le <= KP.LSE_ABS
+
+
+def test_small_head_counts_attention():
+    for H in (1, 4, 20, 48):
+        wl = workloads.custom("heads", 9, (97,), n_heads=H)
+        inp = workloads.indexer_inputs(wl)
+        ql = workloads.q_lat(wl)
+        T = wl.T
+        idx = np.full((T, 128), -1, np.int32)
+        for i in range(T):
+            idx[i, :i + 1] = np.arange(i + 1)
+        out, lse = K.sparse_mla_fwd(ql.cuda(), inp.kv_lat.cuda(), torch.from_numpy(idx).cuda(), wl.scale)
+        out_o, lse_o = O.sparse_attention(ql.float().numpy(), inp.kv_lat.float().numpy(), idx, wl.scale,
+                                          np.arange(T))
+        mx, mean, le = KP.attention_check(out.float().cpu().numpy(), lse.cpu().numpy(), out_o, lse_o)
+        assert mx <= KP.OUT_MAX_ABS and mean <= KP.OUT_MEAN_ABS and le <= KP.LSE_ABS, (H, mx, mean, le)
+
+
+def test_dense_equivalence_below_cutover_on_gpu():
+    """topk >= every document's pool count: GPU rows are the causal prefix of
+    the document and GPU attention equals dense causal attention."""
+    wl = workloads.custom("dense", 13, (700, 321), n_idx_heads=8, d_idx=128, topk=256, n_heads=16)
+    inp = workloads.indexer_inputs(wl)
+    dev = KP.to_dev(inp)
+    res = KP.run_indexer(wl, dev)
+    cu = wl.cu_seqlens
+    for i in range(wl.T):
+        d = 0 if i < cu[1] else 1
+        row = res["indices"][i]
+        assert row[row >= 0].tolist() == list(range(int(cu[d]), i + 1))
+    ql = workloads.q_lat(wl)
+    out, lse = K.sparse_mla_fwd(ql.cuda(), dev["kv_lat"], res["indices_dev"], wl.scale)
+    q = ql.float().double()
+    kv = inp.kv_lat.float().double()
+    ref = torch.zeros_like(q)
+    for d in range(2):
+        s, e = int(cu[d]), int(cu[d + 1])
+        qq = q[s:e].permute(1, 0, 2)
+        kk = kv[s:e][None].expand(wl.n_heads, -1, -1)
+        ref[s:e] = torch.nn.functional.scaled_dot_product_attention(qq, kk, kk, is_causal=True,
+                                                                    scale=wl.scale).permute(1, 0, 2)
+    err = (out.float().cpu().double() - ref).abs()
+    assert err.max() <= KP.OUT_MAX_ABS and err.mean() <= KP.OUT_MEAN_ABS
+
+
+def test_determinism_and_document_isolation():
+    wl = workloads.workload(2)
+    inp = workloads.indexer_inputs(wl)
+    dev = KP.to_dev(inp)
+    a = KP.run_indexer(wl, dev)
+    b = KP.run_indexer(wl, dev)
+    np.testing.assert_array_equal(a["indices"], b["indices"])
+    # perturb the last document: every other document's rows are unchanged
+    s = int(wl.cu_seqlens[-2])
+    dev2 = dict(dev)
+    dev2["q_idx"] = dev["q_idx"].clone()
+    dev2["q_idx"][s:] = -dev2["q_idx"][s:]
+    dev2["k"] = dev["k"].clone()
+    dev2["k"][s:] *= 2
+    c = KP.run_indexer(wl, dev2)
+    np.testing.assert_array_equal(a["indices"][:s], c["indices"][:s])
+    ql = workloads.q_lat(wl).cuda()
+    o1, l1 = K.sparse_mla_fwd(ql, dev["kv_lat"], a["indices_dev"], wl.scale)
+    kv2 = dev["kv_lat"].clone()
+    kv2[s:] = 1.0
+    o2, l2 = K.sparse_mla_fwd(ql, kv2, c["indices_dev"], wl.scale)
+    assert torch.equal(o1[:s], o2[:s]) and torch.equal(l1[:s], l2[:s])
