@@ -42,7 +42,7 @@ def _args():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=3, help="workload index (3 = T=32768 headline)")
-    ap.add_argument("--cpu-rows", type=int, default=96, help="query rows in the CPU-oracle sample")
+    ap.add_argument("--cpu-rows", type=int, default=4096, help="query rows in the CPU-oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 

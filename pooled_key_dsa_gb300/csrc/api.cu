@@ -34,8 +34,12 @@ static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_
 static cudaEvent_t g_stage_events[4];
 static int g_n_stage_events = 0;
 
-static void stage_mark(int k, cudaStream_t s) {
-    if (k < g_n_stage_events) cudaEventRecord(g_stage_events[k], s);
+static int stage_mark(int k, cudaStream_t s) {
+    if (k < g_n_stage_events && cudaEventRecord(g_stage_events[k], s) != cudaSuccess) {
+        cudaGetLastError();
+        return KPOOL_ERR_CUDA;
+    }
+    return KPOOL_OK;
 }
 
 static bool layout_ok(const kpool_layout* L) {
@@ -103,7 +107,7 @@ int dsa_index(const void* q_idx, const float* w, const float* kpool, const kpool
     int32_t* sched = reinterpret_cast<int32_t*>(base + wl.sched);
     float* scores = reinterpret_cast<float*>(base + wl.scores);
     int rc;
-    stage_mark(0, s);
+    if ((rc = stage_mark(0, s)) != KPOOL_OK) return rc;
     if ((rc = launch_index_prep(L, tk, pair_base, sched, s)) != KPOOL_OK) return rc;
     if ((rc = launch_hadamard_fp8(q_idx, true, (int64_t)T * p->n_idx_heads, p->d_idx, nullptr, w, q8, nullptr, ws,
                                   s)) != KPOOL_OK)
@@ -111,14 +115,13 @@ int dsa_index(const void* q_idx, const float* w, const float* kpool, const kpool
     if ((rc = launch_hadamard_fp8(kpool, false, L.max_pools, p->d_idx, L.cu_pools + L.n_docs, nullptr, k8, s_k,
                                   nullptr, s)) != KPOOL_OK)
         return rc;
-    stage_mark(1, s);
+    if ((rc = stage_mark(1, s)) != KPOOL_OK) return rc;
     if ((rc = launch_score(q8, ws, k8, s_k, L, pair_base, sched, tk, p->n_idx_heads, p->d_idx, scores, s)) !=
         KPOOL_OK)
         return rc;
-    stage_mark(2, s);
-    rc = launch_select(scores, pair_base, L, tk, indices, W, s);
-    stage_mark(3, s);
-    return rc;
+    if ((rc = stage_mark(2, s)) != KPOOL_OK) return rc;
+    if ((rc = launch_select(scores, pair_base, L, tk, indices, W, s)) != KPOOL_OK) return rc;
+    return stage_mark(3, s);
 }
 
 int sparse_mla_fwd(const void* q_lat, const void* kv_lat, const int32_t* indices, int32_t W, int32_t T,

@@ -224,6 +224,9 @@ def set_stage_events(events) -> None:
     if not events:
         _check(lib().kpool_set_stage_events(None, 0), "kpool_set_stage_events")
         return
+    for e in events:            # torch creates the CUDA event on first use
+        if not e.cuda_event:
+            e.record()
     arr = (ctypes.c_void_p * len(events))(*[e.cuda_event for e in events])
     _check(lib().kpool_set_stage_events(arr, len(events)), "kpool_set_stage_events")
 
