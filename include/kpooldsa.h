@@ -167,6 +167,27 @@ int sparse_mla_fwd(const void* q_lat, const void* kv_lat, const int32_t* indices
                    int32_t T, int32_t n_heads, float scale, void* out, float* lse,
                    int32_t* status, kpool_stream_t stream);
 
+/* dsa_index_noalloc: dsa_index for callers that cannot allocate.
+ * No counterpart on the pages: this call is an addition of this library.
+ * dsa_index needs a caller-allocated workspace; callers that cannot allocate
+ * device memory (custom-op hosts that hand over only input and output
+ * buffers, runtimes with fixed memory pools, loops that must not call
+ * cudaMalloc because it can block until the device is idle) use this entry
+ * instead.  Arguments and results are those of dsa_index without the
+ * workspace; the scratch is one static device array of 26,349,056 bytes held
+ * by every GPU that loads it until the process exits.
+ * Limits: layout->T <= 4096, layout->n_docs <= 256, n_idx_heads * d_idx <=
+ * 4096; larger sizes return KPOOL_ERR_SHAPE before any launch.
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress); make that first call before any stream capture
+ * begins.  Every call uses the same array and leaves its contents behind
+ * (each call writes every scratch byte it later reads, so nothing needs to
+ * start at zero); calls that can overlap on the GPU (different streams, or
+ * other threads) race on the array and must be serialised by the caller.
+ * It calls no allocator (no cudaMalloc, cudaFree or library allocation). */
+int dsa_index_noalloc(const void* q_idx, const float* w, const float* kpool, const kpool_layout* layout,
+                      int32_t topk, const kpool_params* p, int32_t* indices, int32_t W, kpool_stream_t stream);
+
 /* Stage entry point: top-k select + row expansion alone, fed with scores in
  * the workspace's compact layout (same rules as dsa_index's last step).
  *   scores   fp32, compact triangle as described for kpool_ws_offsets

@@ -21,7 +21,8 @@ ERRORS = {1: "KPOOL_ERR_INVALID_ARG", 2: "KPOOL_ERR_SHAPE", 3: "KPOOL_ERR_ALIGN"
 CODES = {v: k for k, v in ERRORS.items()}
 
 EXPORTED = ("kpool_workspace_bytes", "kpool_workspace_offsets", "kpool_build", "dsa_index", "sparse_mla_fwd",
-            "kpool_stage_select", "kpool_set_stage_events", "kpool_check_status", "kpool_strerror", "kpool_version")
+            "kpool_stage_select", "kpool_set_stage_events", "kpool_check_status", "kpool_strerror", "kpool_version",
+            "dsa_index_noalloc")
 
 
 class KpoolUnavailable(ImportError):
@@ -69,13 +70,15 @@ def lib():
                                 vp]
         L.sparse_mla_fwd.argtypes = [vp, vp, vp, i32, i32, i32, ctypes.c_float, vp, vp, vp, vp]
         L.kpool_stage_select.argtypes = [vp, vp, ctypes.POINTER(LayoutC), i32, vp, i32, vp]
+        L.dsa_index_noalloc.argtypes = [vp, vp, vp, ctypes.POINTER(LayoutC), i32, ctypes.POINTER(Params), vp, i32,
+                                        vp]
         L.kpool_check_status.argtypes = [vp, vp]
         L.kpool_set_stage_events.argtypes = [ctypes.POINTER(ctypes.c_void_p), i32]
         L.kpool_strerror.argtypes = [ctypes.c_int]
         L.kpool_strerror.restype = ctypes.c_char_p
         L.kpool_version.restype = ctypes.c_char_p
         for name in ("kpool_workspace_offsets", "kpool_build", "dsa_index", "sparse_mla_fwd", "kpool_stage_select",
-                     "kpool_set_stage_events", "kpool_check_status"):
+                     "kpool_set_stage_events", "kpool_check_status", "dsa_index_noalloc"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -184,6 +187,24 @@ def dsa_index(q_idx, w, kpool, layout: PoolLayout, topk: int, p: Params, workspa
         indices = torch.empty((T, W), dtype=torch.int32, device=q_idx.device)
     _check(lib().dsa_index(_ptr(q_idx), _ptr(w), _ptr(kpool), ctypes.byref(layout.c), topk, ctypes.byref(p),
                            _ptr(workspace), workspace.numel(), _ptr(indices), W, _stream(stream)), "dsa_index")
+    return indices
+
+
+def dsa_index_noalloc(q_idx, w, kpool, layout: PoolLayout, topk: int, p: Params, indices=None, W=None,
+                      stream=None):
+    """dsa_index without a workspace, for callers that cannot allocate device
+    memory: the library keeps the scratch in one static device array (T up to
+    4096, at most 256 documents).  Only ``indices`` is allocated here, and
+    only when the caller passes none."""
+    T = layout.T
+    _want(q_idx, torch.bfloat16, (T, p.n_idx_heads, p.d_idx), "q_idx")
+    _want(w, torch.float32, (T, p.n_idx_heads), "w")
+    _want(kpool, torch.float32, None, "kpool")
+    W = row_width(topk) if W is None else int(W)
+    if indices is None:
+        indices = torch.empty((T, W), dtype=torch.int32, device=q_idx.device)
+    _check(lib().dsa_index_noalloc(_ptr(q_idx), _ptr(w), _ptr(kpool), ctypes.byref(layout.c), topk,
+                                   ctypes.byref(p), _ptr(indices), W, _stream(stream)), "dsa_index_noalloc")
     return indices
 
 
