@@ -157,7 +157,8 @@ int dsa_index(const void* q_idx, const float* w, const float* kpool, const kpool
  *   indices int32 [T, W]     positions; -1 entries are skipped anywhere in
  *                            the row; entries outside [-1, T) are skipped and
  *                            flagged KPOOL_ERR_INDEX_RANGE in *status.
- *   out    bf16 [T, H, 512]  sum_j softmax_j(scale q.kv_j) kv_j (RNE to bf16)
+ *   out    bf16 [T, H, 512]  sum_j softmax_j(scale q.kv_j) kv_j (RNE to bf16);
+ *                            16-byte aligned
  *   lse    fp32 [T, H]       ln sum_j exp(scale q.kv_j); -inf (and out = 0)
  *                            for a row with no valid slot.
  *   status int32 [1] device error word (may be NULL: errors then go unreported).

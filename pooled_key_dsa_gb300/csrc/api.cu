@@ -108,7 +108,8 @@ int dsa_index(const void* q_idx, const float* w, const float* kpool, const kpool
     float* scores = reinterpret_cast<float*>(base + wl.scores);
     int rc;
     if ((rc = stage_mark(0, s)) != KPOOL_OK) return rc;
-    if ((rc = launch_index_prep(L, tk, pair_base, sched, s)) != KPOOL_OK) return rc;
+    if ((rc = launch_index_prep(L, tk, scoring_group(p->n_idx_heads, p->d_idx), pair_base, sched, s)) != KPOOL_OK)
+        return rc;
     if ((rc = launch_hadamard_fp8(q_idx, true, (int64_t)T * p->n_idx_heads, p->d_idx, nullptr, w, q8, nullptr, ws,
                                   s)) != KPOOL_OK)
         return rc;
@@ -128,7 +129,7 @@ int sparse_mla_fwd(const void* q_lat, const void* kv_lat, const int32_t* indices
                    int32_t n_heads, float scale, void* out, float* lse, int32_t* status, kpool_stream_t stream) {
     if (T < 0 || W < 1 || n_heads < 1 || n_heads > 64) return KPOOL_ERR_SHAPE;
     if (T > 0 && (!q_lat || !kv_lat || !indices || !out || !lse)) return KPOOL_ERR_INVALID_ARG;
-    if (!aligned(q_lat, 16) || !aligned(kv_lat, 16) || !aligned(out, 4) || !aligned(indices, 4))
+    if (!aligned(q_lat, 16) || !aligned(kv_lat, 16) || !aligned(out, 16) || !aligned(indices, 4))
         return KPOOL_ERR_ALIGN;
     if (!(scale == scale)) return KPOOL_ERR_INVALID_ARG;
     return launch_sparse_mla(static_cast<const uint16_t*>(q_lat), static_cast<const uint16_t*>(kv_lat), indices, W, T,

@@ -25,13 +25,24 @@ int launch_kpool_build(const void* k, const float* gate, const float* ape, const
 int launch_hadamard_fp8(const void* x, bool in_bf16, int64_t n_vec, int d, const int32_t* n_valid_dev,
                         const float* w, uint8_t* codes, float* scales, float* ws_out, cudaStream_t stream);
 
-// Per-document score bases and scoring-tile schedule (one tiny kernel).
-int launch_index_prep(const kpool_layout& L, int topk, int64_t* pair_base, int32_t* sched, cudaStream_t stream);
+// Per-document score bases and scoring work schedule (one tiny kernel);
+// qg = scoring_group(n_idx_heads, d_idx).
+int launch_index_prep(const kpool_layout& L, int topk, int qg, int64_t* pair_base, int32_t* sched,
+                      cudaStream_t stream);
+
+// Queries per work item of the tcgen05 scoring kernel (256 / H_i for d_i =
+// 128), or 0 when the mma.sync kernel serves the shape (d_i = 64).
+int scoring_group(int n_idx_heads, int d_idx);
 
 // FP8 pool scores into the compact triangle.
 int launch_score(const uint8_t* q8, const float* ws, const uint8_t* k8, const float* s_k, const kpool_layout& L,
                  const int64_t* pair_base, const int32_t* sched, int topk, int n_idx_heads, int d_idx,
                  float* scores, cudaStream_t stream);
+
+// The mma.sync e4m3 scoring kernel (d_i = 64 shapes).
+int launch_score_mma(const uint8_t* q8, const float* ws, const uint8_t* k8, const float* s_k, const kpool_layout& L,
+                     const int64_t* pair_base, const int32_t* sched, int topk, int n_idx_heads, int d_idx,
+                     float* scores, cudaStream_t stream);
 
 // Top-k select, expansion to positions, own tail, -1 padding.
 int launch_select(const float* scores, const int64_t* pair_base, const kpool_layout& L, int topk, int32_t* indices,

@@ -1,4 +1,5 @@
-// FP8 pool scoring ("lightning indexer" over pools) and its tile schedule.
+// FP8 pool scoring for d_i = 64 (mma.sync e4m3) and the scoring schedule.
+// The d_i = 128 shapes run on the tcgen05 kernel in score_tc.cu.
 //
 // prime-rl PR "GLM-5.3-Flash text model", Summary: each query scores the
 // complete pools of its own document that end at or before it, reusing an FP8
@@ -55,10 +56,14 @@ __device__ __forceinline__ DocTiles doc_tiles(int L, int topk) {
 }  // namespace
 
 // One block: pair_base[d] (start of document d's score triangle) and
-// sched[d] (first tile of document d); sched[n_docs] = total tiles.
+// sched[d] (first work item of document d); sched[n_docs] = total items.
+// qg = 0: items are the (16 queries x 64 pools) tiles of the mma.sync kernel;
+// qg > 0: items are groups of qg consecutive queries (tcgen05 kernel), from
+// the group holding r = 4*topk + 3 to the end of the document.
 __global__ void __launch_bounds__(1024) index_prep_kernel(const int32_t* __restrict__ cu_seqlens,
                                                           const int32_t* __restrict__ cu_pools, int n_docs, int topk,
-                                                          int64_t* __restrict__ pair_base, int32_t* __restrict__ sched) {
+                                                          int qg, int64_t* __restrict__ pair_base,
+                                                          int32_t* __restrict__ sched) {
     __shared__ int64_t wsum_p[32], wsum_t[32];
     __shared__ int64_t carry_p, carry_t;
     const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, nw = blockDim.x >> 5;
@@ -71,7 +76,12 @@ __global__ void __launch_bounds__(1024) index_prep_kernel(const int32_t* __restr
         if (ok && d < n_docs) {
             const int L = cu_seqlens[d + 1] - cu_seqlens[d];
             vp = pairs_before(L);
-            vt = doc_tiles(L, topk).count;
+            if (qg > 0) {
+                const int q_all = (L + qg - 1) / qg, q0 = (KPOOL * topk + KPOOL - 1) / qg;
+                vt = q_all > q0 ? q_all - q0 : 0;
+            } else {
+                vt = doc_tiles(L, topk).count;
+            }
         }
         int64_t xp = vp, xt = vt;
         for (int o = 1; o < 32; o <<= 1) {
@@ -203,8 +213,9 @@ __global__ void __launch_bounds__(128) score_kernel(const uint8_t* __restrict__ 
     }
 }
 
-int launch_index_prep(const kpool_layout& L, int topk, int64_t* pair_base, int32_t* sched, cudaStream_t stream) {
-    index_prep_kernel<<<1, 1024, 0, stream>>>(L.cu_seqlens, L.cu_pools, L.n_docs, topk, pair_base, sched);
+int launch_index_prep(const kpool_layout& L, int topk, int qg, int64_t* pair_base, int32_t* sched,
+                      cudaStream_t stream) {
+    index_prep_kernel<<<1, 1024, 0, stream>>>(L.cu_seqlens, L.cu_pools, L.n_docs, topk, qg, pair_base, sched);
     return cudaGetLastError() == cudaSuccess ? KPOOL_OK : KPOOL_ERR_CUDA;
 }
 
@@ -216,19 +227,14 @@ static void launch_score_t(const uint8_t* q8, const float* ws, const uint8_t* k8
                                                       L.max_pools, pair_base, sched, topk, scores);
 }
 
-int launch_score(const uint8_t* q8, const float* ws, const uint8_t* k8, const float* s_k, const kpool_layout& L,
-                 const int64_t* pair_base, const int32_t* sched, int topk, int n_idx_heads, int d_idx,
-                 float* scores, cudaStream_t stream) {
+int launch_score_mma(const uint8_t* q8, const float* ws, const uint8_t* k8, const float* s_k, const kpool_layout& L,
+                     const int64_t* pair_base, const int32_t* sched, int topk, int n_idx_heads, int d_idx,
+                     float* scores, cudaStream_t stream) {
 #define KPOOL_SCORE_CASE(H, D)                                                                   \
     if (n_idx_heads == H && d_idx == D) {                                                        \
         launch_score_t<H, D>(q8, ws, k8, s_k, L, pair_base, sched, topk, scores, stream);        \
         return cudaGetLastError() == cudaSuccess ? KPOOL_OK : KPOOL_ERR_CUDA;                    \
     }
-    KPOOL_SCORE_CASE(32, 128)
-    KPOOL_SCORE_CASE(64, 128)
-    KPOOL_SCORE_CASE(16, 128)
-    KPOOL_SCORE_CASE(8, 128)
-    KPOOL_SCORE_CASE(4, 128)
     KPOOL_SCORE_CASE(32, 64)
     KPOOL_SCORE_CASE(16, 64)
     KPOOL_SCORE_CASE(8, 64)

@@ -1,0 +1,350 @@
+// FP8 pool scoring on tcgen05 (d_i = 128).
+//
+// prime-rl PR "GLM-5.3-Flash text model", Summary: each query scores the
+// complete pools of its own document that end at or before it with an FP8
+// indexer over pools: S[i,p] = s_k[p] * sum_h ws[i,h] * ReLU(q8[i,h] . k8[p]),
+// ws = w * s_q (miles "GLM-5.3-Flash" recipe, section 1: kpool-compressed
+// lightning indexer).
+//
+// Work item = a group of QG = 256 / H_i consecutive queries of one document
+// (from the group holding r = 4*topk + 3 on; earlier rows keep every pool).
+// Per item the (query, head) rows form the MMA's N = 256 operand (TMA, one
+// 32 KB box); the item's pools stream through a 6-stage ring of 128-pool A
+// tiles (TMA, 16 KB).  Each tile is 4 tcgen05 kind::f8f6f4 MMAs (M = 128
+// pools, N = 256, K = 32) into one of two TMEM accumulators, so the epilogue
+// of tile t overlaps the MMAs of tile t+1.
+//
+// Epilogue: 8 warps, two per TMEM subpartition; a thread owns one pool (its
+// TMEM lane) and half of the columns, so ReLU, the head weights and the head
+// sum stay thread-local; one coalesced store per (query, pool).
+// Items are spread over the persistent CTAs in a snake order (the item size
+// grows along a document).  Waits are bounded (KPOOL_ERR_TIMEOUT).
+#include <cstdint>
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "kpool_common.cuh"
+#include "kpool_launch.h"
+#include "tc_ptx.cuh"
+
+namespace kpool {
+
+namespace {
+
+constexpr int SC_THREADS = 384;        // warp 0 TMA, warp 1 MMA, warps 4-11 epilogue
+constexpr int A_STAGES = 6;
+constexpr int A_BYTES = 128 * 128;     // 128 pools x 128 B
+constexpr int B_BYTES = 256 * 128;     // 256 (query, head) rows x 128 B
+constexpr int OFF_B = 0;
+constexpr int OFF_A = OFF_B + 2 * B_BYTES;
+constexpr int OFF_WS = OFF_A + A_STAGES * A_BYTES;
+constexpr int OFF_SMALL = OFF_WS + 2 * 256 * 4;
+
+struct ScSmall {
+    uint64_t b_full[2], b_empty[2], a_full[A_STAGES], a_empty[A_STAGES], acc_full[2], acc_empty[2], drain;
+    int abort;
+    uint32_t tmem;
+};
+constexpr int SC_SMEM = OFF_SMALL + (int)sizeof(ScSmall) + 1024;
+
+constexpr uint32_t ID_SC = tc::idesc(128, 256, 0, 0, false, false);   // e4m3 x e4m3 -> fp32
+
+struct Item {
+    int d, s_d, L, p0, r0, ntiles;
+};
+
+__device__ __forceinline__ Item decode_item(int j, const int32_t* sched, const int32_t* cu_seqlens,
+                                            const int32_t* cu_pools, int n_docs, int topk, int qg) {
+    int lo = 0, hi = n_docs - 1;                 // largest d with sched[d] <= j
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (sched[mid] <= j) lo = mid; else hi = mid - 1;
+    }
+    Item it;
+    it.d = lo;
+    it.s_d = cu_seqlens[lo];
+    it.L = cu_seqlens[lo + 1] - it.s_d;
+    it.p0 = cu_pools[lo];
+    it.r0 = ((KPOOL * topk + KPOOL - 1) / qg + (j - sched[lo])) * qg;
+    const int r_last = min(it.r0 + qg - 1, it.L - 1);
+    const int nmax = (r_last + 1) / KPOOL;
+    it.ntiles = (nmax + 127) / 128;
+    return it;
+}
+
+// k-th item of this CTA in snake order over the grid (balances growing items)
+__device__ __forceinline__ int item_of(int k) {
+    const int G = gridDim.x, c = blockIdx.x;
+    return k * G + ((k & 1) ? (G - 1 - c) : c);
+}
+
+__device__ __forceinline__ bool warp_wait(uint32_t addr, uint32_t parity, const volatile int* abort) {
+    uint32_t ok = 0;
+    if ((threadIdx.x & 31) == 0) ok = tc::mbar_wait(addr, parity, abort) ? 1u : 0u;
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
+// Named barrier 1 over the 256 epilogue threads, ORing a predicate.
+__device__ __forceinline__ bool epi_or(bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, 1, 256, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+        : "=r"(r)
+        : "r"((uint32_t)pred)
+        : "memory");
+    return r != 0;
+}
+
+}  // namespace
+
+template <int HI>
+__global__ void __launch_bounds__(SC_THREADS, 1) score_tc_kernel(
+    const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k, const float* __restrict__ ws,
+    const float* __restrict__ s_k, const int32_t* __restrict__ cu_seqlens, const int32_t* __restrict__ cu_pools,
+    int n_docs, int max_pools, int T, const int64_t* __restrict__ pair_base, const int32_t* __restrict__ sched,
+    int topk, uint32_t b_box_bytes, uint32_t a_box_bytes, float* __restrict__ scores, int32_t* status) {
+    constexpr int QG = 256 / HI;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
+    ScSmall& sm = *reinterpret_cast<ScSmall*>(smem + OFF_SMALL);
+    const uint32_t s_base = tc::smem_u32(smem);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    volatile int* abort_flag = &sm.abort;
+    const int total = sched[n_docs];
+
+    if (tid == 0) {
+        for (int b = 0; b < 2; ++b) {
+            tc::mbar_init(tc::smem_u32(&sm.b_full[b]), 1);
+            tc::mbar_init(tc::smem_u32(&sm.b_empty[b]), 1);
+            tc::mbar_init(tc::smem_u32(&sm.acc_full[b]), 1);
+            tc::mbar_init(tc::smem_u32(&sm.acc_empty[b]), 8);
+        }
+        for (int s = 0; s < A_STAGES; ++s) {
+            tc::mbar_init(tc::smem_u32(&sm.a_full[s]), 1);
+            tc::mbar_init(tc::smem_u32(&sm.a_empty[s]), 1);
+        }
+        tc::mbar_init(tc::smem_u32(&sm.drain), 1);
+        sm.abort = 0;
+        tc::mbar_init_fence();
+    }
+    if (warp == 1) tc::tmem_alloc(tc::smem_u32(&sm.tmem), 512);
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tmem = sm.tmem;
+
+    if (warp == 0) {
+        // ===================================================== TMA producer
+        if (lane == 0) {
+            uint32_t ni = 0, na = 0;
+            bool ok = true;
+            for (int k = 0; ok; ++k, ++ni) {
+                const int j = item_of(k);
+                if (j >= total) break;
+                const Item it = decode_item(j, sched, cu_seqlens, cu_pools, n_docs, topk, QG);
+                const int ib = ni & 1;
+                if (!tc::mbar_wait(tc::smem_u32(&sm.b_empty[ib]), ((ni >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
+                tc::mbar_arrive_expect_tx(tc::smem_u32(&sm.b_full[ib]), b_box_bytes);
+                tc::tma_load_2d(s_base + OFF_B + ib * B_BYTES, &tmap_q, 0, (it.s_d + it.r0) * HI,
+                                tc::smem_u32(&sm.b_full[ib]));
+                for (int t = 0; t < it.ntiles; ++t, ++na) {
+                    const int as = na % A_STAGES;
+                    if (!tc::mbar_wait(tc::smem_u32(&sm.a_empty[as]), ((na / A_STAGES) & 1) ^ 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc::mbar_arrive_expect_tx(tc::smem_u32(&sm.a_full[as]), a_box_bytes);
+                    tc::tma_load_2d(s_base + OFF_A + as * A_BYTES, &tmap_k, 0, it.p0 + 128 * t,
+                                    tc::smem_u32(&sm.a_full[as]));
+                }
+            }
+            if (!ok) {
+                sm.abort = 1;
+                set_status(status, KPOOL_ERR_TIMEOUT);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        // ===================================================== MMA issuer
+        if (lane == 0) {
+            uint32_t ni = 0, na = 0, nacc = 0;
+            bool ok = true;
+            for (int k = 0; ok && !*abort_flag; ++k, ++ni) {
+                const int j = item_of(k);
+                if (j >= total) break;
+                const Item it = decode_item(j, sched, cu_seqlens, cu_pools, n_docs, topk, QG);
+                const int ib = ni & 1;
+                if (!tc::mbar_wait(tc::smem_u32(&sm.b_full[ib]), (ni >> 1) & 1, abort_flag)) { ok = false; break; }
+                const uint64_t bd = tc::sw128_desc(s_base + OFF_B + ib * B_BYTES, 0, 1024);
+                for (int t = 0; t < it.ntiles; ++t, ++na, ++nacc) {
+                    const int as = na % A_STAGES, ab = nacc & 1;
+                    if (!tc::mbar_wait(tc::smem_u32(&sm.a_full[as]), (na / A_STAGES) & 1, abort_flag) ||
+                        !tc::mbar_wait(tc::smem_u32(&sm.acc_empty[ab]), ((nacc >> 1) & 1) ^ 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc::fence_after();
+                    const uint64_t ad = tc::sw128_desc(s_base + OFF_A + as * A_BYTES, 0, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        tc::mma_e4m3(tmem + 256 * ab, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), ID_SC,
+                                     kk > 0 ? 1u : 0u);
+                    tc::commit(tc::smem_u32(&sm.a_empty[as]));
+                    tc::commit(tc::smem_u32(&sm.acc_full[ab]));
+                }
+                if (!ok) break;
+                tc::commit(tc::smem_u32(&sm.b_empty[ib]));
+            }
+            if (!ok) {
+                sm.abort = 1;
+                set_status(status, KPOOL_ERR_TIMEOUT);
+            }
+            tc::commit(tc::smem_u32(&sm.drain));
+            const uint64_t t0 = tc::globaltimer_ns();
+            while (!tc::mbar_try(tc::smem_u32(&sm.drain), 0) && tc::globaltimer_ns() - t0 < tc::WAIT_LIMIT_NS) {
+            }
+        }
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ===================================================== epilogue
+        const int e = tid - 128;                      // 0..255
+        const int sp = warp & 3;                      // TMEM subpartition (lanes 32sp..)
+        const int ch = (warp - 4) >> 2;               // column half: queries ch*QG/2 ..
+        const uint32_t lane_base = (uint32_t)(sp * 32) << 16;
+        uint32_t ni = 0, nacc = 0;
+        bool bad = false;
+        for (int k = 0;; ++k, ++ni) {
+            const int j = item_of(k);
+            if (j >= total) break;
+            const Item it = decode_item(j, sched, cu_seqlens, cu_pools, n_docs, topk, QG);
+            const int i0 = it.s_d + it.r0;
+            // the item's head weights (256 floats) into shared memory
+            float* wsb = reinterpret_cast<float*>(smem + OFF_WS) + (ni & 1) * 256;
+            wsb[e] = (it.r0 + e / HI < it.L) ? ws[(int64_t)i0 * HI + e] : 0.f;
+            if (epi_or(bad)) { bad = true; break; }
+            const int64_t row_base = pair_base[it.d];
+            for (int t = 0; t < it.ntiles; ++t, ++nacc) {
+                const int ab = nacc & 1;
+                bad = bad || !warp_wait(tc::smem_u32(&sm.acc_full[ab]), (nacc >> 1) & 1, abort_flag);
+                if (bad) continue;
+                tc::fence_after();
+                const int pool_local = 128 * t + 32 * sp + lane;
+                const int pool = it.p0 + pool_local;
+                const float sk = pool < max_pools ? s_k[pool] : 0.f;
+                float acc[QG / 2];
+#pragma unroll
+                for (int q = 0; q < QG / 2; ++q) acc[q] = 0.f;
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    uint32_t v[32];
+                    tc::tmem_ld32(tmem + 256 * ab + lane_base + ch * 128 + cc * 32, v);
+                    tc::tmem_wait_ld();
+#pragma unroll
+                    for (int jj = 0; jj < 32; ++jj) {
+                        const int col = ch * 128 + cc * 32 + jj;                 // (query, head) column
+                        acc[(cc * 32 + jj) / HI] += wsb[col] * fmaxf(__uint_as_float(v[jj]), 0.f);
+                    }
+                }
+                tc::fence_before();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(tc::smem_u32(&sm.acc_empty[ab]));
+#pragma unroll
+                for (int q = 0; q < QG / 2; ++q) {
+                    const int r = it.r0 + ch * (QG / 2) + q;
+                    const int n_i = (r + 1) / KPOOL;
+                    if (r < it.L && n_i > topk && pool_local < n_i)
+                        scores[row_base + pairs_before(r) + pool_local] = acc[q] * sk;
+                }
+            }
+        }
+        if (bad) {
+            sm.abort = 1;
+            set_status(status, KPOOL_ERR_TIMEOUT);
+        }
+    }
+    tc::fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc::fence_after();
+        tc::tmem_dealloc(tmem, 512);
+    }
+}
+
+int scoring_group(int n_idx_heads, int d_idx) {
+    if (d_idx != 128) return 0;
+    switch (n_idx_heads) {
+        case 4: case 8: case 16: case 32: case 64: return 256 / n_idx_heads;
+        default: return 0;
+    }
+}
+
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// 2-D byte tensor [rows, 128] with 128-byte rows, 128-byte swizzle, box
+// {128, box_rows}.
+static bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {128, rows};
+    const cuuint64_t strides[1] = {128};
+    const cuuint32_t box[2] = {128, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int HI>
+static int launch_tc(const uint8_t* q8, const float* ws, const uint8_t* k8, const float* s_k, const kpool_layout& L,
+                     const int64_t* pair_base, const int32_t* sched, int topk, float* scores, cudaStream_t stream) {
+    static int n_sm[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return KPOOL_ERR_CUDA;
+    if (n_sm[dev] == 0) {
+        if (cudaFuncSetAttribute(score_tc_kernel<HI>, cudaFuncAttributeMaxDynamicSharedMemorySize, SC_SMEM) !=
+            cudaSuccess)
+            return KPOOL_ERR_CUDA;
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return KPOOL_ERR_CUDA;
+        n_sm[dev] = sms;
+    }
+    const uint64_t q_rows = (uint64_t)L.T * HI;
+    const uint64_t k_rows = (uint64_t)(L.max_pools > 0 ? L.max_pools : 1);
+    const uint32_t b_rows = (uint32_t)(q_rows < 256 ? q_rows : 256);
+    const uint32_t a_rows = (uint32_t)(k_rows < 128 ? k_rows : 128);
+    CUtensorMap mq, mk;
+    if (!make_map(&mq, q8, q_rows, b_rows) || !make_map(&mk, k8, k_rows, a_rows)) return KPOOL_ERR_CUDA;
+    score_tc_kernel<HI><<<n_sm[dev], SC_THREADS, SC_SMEM, stream>>>(
+        mq, mk, ws, s_k, L.cu_seqlens, L.cu_pools, L.n_docs, L.max_pools, L.T, pair_base, sched, topk, b_rows * 128,
+        a_rows * 128, scores, L.status);
+    return cudaGetLastError() == cudaSuccess ? KPOOL_OK : KPOOL_ERR_CUDA;
+}
+
+int launch_score(const uint8_t* q8, const float* ws, const uint8_t* k8, const float* s_k, const kpool_layout& L,
+                 const int64_t* pair_base, const int32_t* sched, int topk, int n_idx_heads, int d_idx,
+                 float* scores, cudaStream_t stream) {
+    if (L.T <= 0) return KPOOL_OK;
+    if (scoring_group(n_idx_heads, d_idx) == 0)
+        return launch_score_mma(q8, ws, k8, s_k, L, pair_base, sched, topk, n_idx_heads, d_idx, scores, stream);
+    switch (n_idx_heads) {
+        case 4: return launch_tc<4>(q8, ws, k8, s_k, L, pair_base, sched, topk, scores, stream);
+        case 8: return launch_tc<8>(q8, ws, k8, s_k, L, pair_base, sched, topk, scores, stream);
+        case 16: return launch_tc<16>(q8, ws, k8, s_k, L, pair_base, sched, topk, scores, stream);
+        case 32: return launch_tc<32>(q8, ws, k8, s_k, L, pair_base, sched, topk, scores, stream);
+        case 64: return launch_tc<64>(q8, ws, k8, s_k, L, pair_base, sched, topk, scores, stream);
+        default: return KPOOL_ERR_SHAPE;
+    }
+}
+
+}  // namespace kpool

@@ -1,81 +1,95 @@
-// Sparse latent attention forward (absorbed NoPE MLA over index rows).
+// Sparse latent attention forward (absorbed NoPE MLA over index rows), tcgen05.
 //
 // NeMo AutoModel PR "add GLM-5.3-Flash training support", Changelog: the K
 // projection is absorbed into the query and attention runs over the shared
-// 512-wide latent, which is both key and value; the V projection is applied
-// afterwards by the caller.  miles "GLM-5.3-Flash" recipe, section 1: NoPE
-// MLA with 64 heads.
+// 512-wide latent, which is both key and value; the caller applies the V
+// projection afterwards.  miles "GLM-5.3-Flash" recipe, section 1: NoPE MLA,
+// 64 heads.
 //
-// One CTA per query token, all heads at once (heads are the MMA M dimension).
-// The index row is walked in blocks of 64 slots; each block's latent rows are
-// gathered with cp.async into a double-buffered, XOR-swizzled shared tile
-// while the previous block computes.  S = Q K^T and O += P V run on bf16
-// tensor-core MMAs (m16n8k16, fp32 accumulate); the online softmax keeps the
-// running max and sum per head in shared memory and uses base-2 exponentials
-// on logits pre-multiplied by scale*log2(e).
+// Persistent CTAs (one per SM), each walking query tokens i = blockIdx.x +
+// k*gridDim.x.  For one query the index row is cut into blocks of 32 slots:
+//   S   = Q Kv^T      tcgen05 kind::f16, M = 64 heads, N = 32 slots, K = 512
+//   O^T += Kv^T P^T   tcgen05 kind::f16, M = 128 latent rows (4 tiles),
+//                     N = 64 heads, K = 32 slots; A is the gathered block read
+//                     MN-major, so the tile that fed S also feeds PV
+// Q (64 KB) stays in shared memory for the whole query; gathered latent rows
+// go through a 4-stage ring of 32 KB blocks; S (2 x 32 columns) and O^T
+// (4 x 64 columns) live in TMEM.
+//
+// Warp roles (256 threads):
+//   warp 0     producer: index scan, Q and latent-row gathers (cp.async 16 B,
+//              128-byte swizzle written by hand), mbarrier hand-off
+//   warp 2     TMEM owner; lane 0 issues S over latent 0..255 and every PV
+//   warp 3     lane 0 issues S over latent 256..511 into a second
+//              accumulator (one thread cannot issue MMAs fast enough for
+//              these small shapes); the softmax adds the two halves
+//   warps 4-7  softmax: the M=64 accumulator sits in lanes 0-15 of each
+//              warp's TMEM subpartition; after the load, lanes 16-31 take the
+//              upper half of every row's slots, so all 32 lanes work.  Lazy
+//              rescale of O^T only when a head's running max grows by more
+//              than 2^8; P^T to shared memory in the operand layout; epilogue
+//              O^T / l -> bf16
+// Every wait is bounded and warp-uniform (lane 0 polls, the warp takes its
+// answer); on expiry the kernel records KPOOL_ERR_TIMEOUT, the softmax warps
+// agree on stopping at their next named barrier, every role leaves its loop,
+// in-flight copies and MMAs are drained and TMEM is freed.
 #include <cstdint>
 
 #include "kpool_common.cuh"
 #include "kpool_launch.h"
+#include "tc_ptx.cuh"
 
 namespace kpool {
 
 namespace {
 
-constexpr int MLA_THREADS = 256;
-constexpr int BN = 64;                       // slots per block
-constexpr int HP = 64;                       // padded head rows
-constexpr int ROW_BYTES = D_LAT * 2;         // 1024
-constexpr int S_STRIDE = BN + 4;             // fp32 row stride of the score tile
+constexpr int BN = 32;                 // slots per block
+constexpr int NSTAGE = 4;              // latent-row ring depth
+constexpr int NSB = 2;                 // S / P double buffers
+constexpr int HP = 64;                 // head rows (M of S, N of PV)
+constexpr float TAU = 8.0f;            // lazy-rescale threshold (log2 units)
+constexpr int THREADS = 256;
 
-struct MlaSmem {
-    uint8_t q[HP * ROW_BYTES];               // 64 KB, swizzled
-    uint8_t kv[2][BN * ROW_BYTES];           // 2 x 64 KB, swizzled
-    float s[HP * S_STRIDE];                  // 17 KB
-    uint8_t p[HP * BN * 2];                  // 8 KB bf16, swizzled
-    int32_t idx[2][BN];
-    int32_t any_valid[2];
-    float m[HP], l[HP], alpha[HP];
+constexpr int Q_BYTES = HP * D_LAT * 2;          // 64 KB: 8 chunks x [64 rows x 128 B]
+constexpr int Q_CHUNK = HP * 128;                // 8 KB
+constexpr int KV_BYTES = BN * D_LAT * 2;         // 32 KB: 8 chunks x [32 rows x 128 B]
+constexpr int KV_CHUNK = BN * 128;               // 4 KB
+constexpr int P_BYTES = HP * 128;                // 8 KB: [64 head rows x 128 B] (first 64 B used)
+constexpr int STAGE_BYTES = 4 * HP * 64;         // 16 KB epilogue staging (4 warps x 64 heads x 32 bf16)
+
+constexpr int OFF_Q = 0;
+constexpr int OFF_KV = OFF_Q + Q_BYTES;
+constexpr int OFF_P = OFF_KV + NSTAGE * KV_BYTES;
+constexpr int OFF_STAGE = OFF_P + NSB * P_BYTES;
+constexpr int OFF_SMALL = OFF_STAGE + STAGE_BYTES;
+
+struct Small {
+    uint64_t q_full, q_empty, o_full, o_free, drain;
+    uint64_t kv_full[NSTAGE], kv_empty[NSTAGE];
+    uint64_t s_full[NSB], s_free[NSB], p_full[NSB], p_empty[NSB], o_step[NSB];
+    uint32_t mask[NSTAGE];
+    int nb;
+    int abort;
+    uint32_t tmem;
+    float alpha[2][HP];
+    float inv_l[HP];
 };
+constexpr int SMEM_BYTES = OFF_SMALL + (int)sizeof(Small) + 1024;   // + alignment slack
 
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
+constexpr uint32_t TM_O = 0;           // O^T tile t at columns 64t
+constexpr uint32_t TM_S = 256;         // S buffer b, half k (latent 256k..256k+255) at 256 + 64b + 32k
+constexpr uint32_t TM_COLS = 512;
 
-// 1024-byte rows of 64 16-byte chunks; chunk c of row r lives at c ^ (r & 7).
-__device__ __forceinline__ uint32_t swz1k(int row, int chunk) {
-    return (uint32_t)(row * ROW_BYTES + ((chunk ^ (row & 7)) << 4));
-}
-// 128-byte rows of 8 chunks.
-__device__ __forceinline__ uint32_t swz128(int row, int chunk) {
-    return (uint32_t)(row * 128 + ((chunk ^ (row & 7)) << 4));
-}
+constexpr uint32_t ID_S = tc::idesc(64, BN, 1, 1, false, false);
+constexpr uint32_t ID_PV = tc::idesc(128, HP, 1, 1, true, false);
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, bool valid) {
-    const int n = valid ? 16 : 0;
-    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src), "r"(n));
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N)); }
+__device__ __forceinline__ uint32_t swz(int row, int unit) { return (uint32_t)(row * 128 + ((unit ^ (row & 7)) << 4)); }
 
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
-    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];\n"
-                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
-                 : "r"(addr));
-}
-__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
-                                               uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-        "{%0,%1,%2,%3};\n"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+// 2^x on the SFU (ex2.approx.ftz: relative error near 2^-22; -inf -> +0).
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+    return y;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
@@ -83,235 +97,410 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     return *reinterpret_cast<const uint32_t*>(&v);
 }
 
+__device__ __forceinline__ void fail(Small& sm, int32_t* status) {
+    sm.abort = 1;
+    set_status(status, KPOOL_ERR_TIMEOUT);
+}
+
+// Named barrier 2 over the 128 softmax threads that also ORs a predicate:
+// every thread gets the same answer, so decisions taken on it stay uniform.
+__device__ __forceinline__ bool wg_or(bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, 2, 128, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+        : "=r"(r)
+        : "r"((uint32_t)pred)
+        : "memory");
+    return r != 0;
+}
+
+// Warp-uniform bounded wait: lane 0 polls, every lane gets the answer.
+__device__ __forceinline__ bool warp_wait(uint32_t addr, uint32_t parity, const volatile int* abort) {
+    uint32_t ok = 0;
+    if ((threadIdx.x & 31) == 0) ok = tc::mbar_wait(addr, parity, abort) ? 1u : 0u;
+    return __shfl_sync(0xffffffffu, ok, 0) != 0;
+}
+
 }  // namespace
 
-template <int MT>
-__global__ void __launch_bounds__(MLA_THREADS, 1) sparse_mla_kernel(const uint16_t* __restrict__ q_lat,
-                                                                   const uint16_t* __restrict__ kv_lat,
-                                                                   const int32_t* __restrict__ indices, int W, int T,
-                                                                   int H, float scale_log2, uint16_t* __restrict__ out,
-                                                                   float* __restrict__ lse, int32_t* status) {
+__global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_t* __restrict__ q_lat,
+                                                                  const uint16_t* __restrict__ kv_lat,
+                                                                  const int32_t* __restrict__ indices, int W, int T,
+                                                                  int H, float scale_log2,
+                                                                  uint16_t* __restrict__ out,
+                                                                  float* __restrict__ lse, int32_t* status) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
-    MlaSmem& sm = *reinterpret_cast<MlaSmem*>(smem_raw);
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int g = lane >> 2, tig = lane & 3;
-    const int i = blockIdx.x;
-    const int32_t* irow = indices + (int64_t)i * W;
-    const int nblk = (W + BN - 1) / BN;
-    const uint32_t q_base = smem_u32(sm.q);
-    const uint32_t kv_base[2] = {smem_u32(sm.kv[0]), smem_u32(sm.kv[1])};
-    const uint32_t p_base = smem_u32(sm.p);
+    uint8_t* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
+    Small& sm = *reinterpret_cast<Small*>(smem + OFF_SMALL);
+    const uint32_t s_base = tc::smem_u32(smem);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    volatile int* abort_flag = &sm.abort;
 
-    // ---- Q tile (rows >= H are zero) and running statistics
-    {
-        const uint16_t* qsrc = q_lat + (int64_t)i * H * D_LAT;
-        for (int c = tid; c < HP * 64; c += MLA_THREADS) {
-            const int row = c >> 6, ch = c & 63;
-            const bool v = row < H;
-            cp_async16(q_base + swz1k(row, ch), v ? qsrc + row * D_LAT + ch * 8 : q_lat, v);
+    if (tid == 0) {
+        tc::mbar_init(tc::smem_u32(&sm.q_full), 1);
+        tc::mbar_init(tc::smem_u32(&sm.q_empty), 3);      // two MMA issuers + softmax acknowledgement
+        tc::mbar_init(tc::smem_u32(&sm.o_full), 1);
+        tc::mbar_init(tc::smem_u32(&sm.o_free), 4);
+        tc::mbar_init(tc::smem_u32(&sm.drain), 2);
+        for (int s = 0; s < NSTAGE; ++s) {
+            tc::mbar_init(tc::smem_u32(&sm.kv_full[s]), 1);
+            tc::mbar_init(tc::smem_u32(&sm.kv_empty[s]), 2);    // S-half issuer + PV issuer
         }
+        for (int b = 0; b < NSB; ++b) {
+            tc::mbar_init(tc::smem_u32(&sm.s_full[b]), 2);      // both halves of S
+            tc::mbar_init(tc::smem_u32(&sm.s_free[b]), 4);
+            tc::mbar_init(tc::smem_u32(&sm.p_full[b]), 4);
+            tc::mbar_init(tc::smem_u32(&sm.p_empty[b]), 1);
+            tc::mbar_init(tc::smem_u32(&sm.o_step[b]), 1);
+        }
+        sm.abort = 0;
+        tc::mbar_init_fence();
     }
-    if (tid < HP) {
-        sm.m[tid] = -INFINITY;
-        sm.l[tid] = 0.f;
-    }
+    if (warp == 2) tc::tmem_alloc(tc::smem_u32(&sm.tmem), TM_COLS);
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    const uint32_t tmem = sm.tmem;
 
-    auto load_idx = [&](int blk, int buf) {
-        int valid = 0;
-        if (tid < BN) {
-            const int slot = blk * BN + tid;
-            int v = slot < W ? irow[slot] : -1;
-            if (v < -1 || v >= T) {
-                set_status(status, KPOOL_ERR_INDEX_RANGE);
-                v = -1;
+    if (warp == 0) {
+        // ===================================================== producer (one warp)
+        uint32_t g = 0;                             // global block counter
+        uint32_t qn = 0;
+        bool ok = true;
+        for (int i = blockIdx.x; i < T && ok; i += gridDim.x, ++qn) {
+            if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
+            const int32_t* irow = indices + (int64_t)i * W;
+            // last valid slot of the row (entries outside [-1, T) are flagged and skipped)
+            int last = -1;
+            for (int j = lane; j < W; j += 32) {
+                const int v = irow[j];
+                if (v >= 0 && v < T) last = j;
+                else if (v != -1) set_status(status, KPOOL_ERR_INDEX_RANGE);
             }
-            sm.idx[buf][tid] = v;
-            valid = v >= 0;
-        }
-        valid = __syncthreads_or(valid);
-        if (tid == 0) sm.any_valid[buf] = valid;
-    };
-    auto load_kv = [&](int buf) {
-        const int ch = tid & 63;
-        for (int row = tid >> 6; row < BN; row += MLA_THREADS / 64) {
-            const int v = sm.idx[buf][row];
-            cp_async16(kv_base[buf] + swz1k(row, ch), v >= 0 ? kv_lat + (int64_t)v * D_LAT + ch * 8 : kv_lat,
-                       v >= 0);
-        }
-    };
-
-    load_idx(0, 0);
-    load_kv(0);
-    cp_async_commit();
-
-    float o[32][4];
-#pragma unroll
-    for (int n = 0; n < 32; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
-    const int mt = warp & 3, half = warp >> 2;
-
-    for (int blk = 0; blk < nblk; ++blk) {
-        const int buf = blk & 1;
-        if (blk + 1 < nblk) {
-            load_idx(blk + 1, buf ^ 1);
-            load_kv(buf ^ 1);
-            cp_async_commit();
-            cp_async_wait<1>();
-        } else {
-            cp_async_wait<0>();
-        }
-        __syncthreads();
-        if (!sm.any_valid[buf]) continue;          // uniform across the block
-
-        // ---- S = Q K^T for 16 heads x 32 slots per warp
-        if (mt < MT) {
-            float acc[4][4];
-#pragma unroll
-            for (int n = 0; n < 4; ++n) acc[n][0] = acc[n][1] = acc[n][2] = acc[n][3] = 0.f;
+            for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
+            const int nb = (last + BN) / BN;
+            // Q tile: the previous query's S MMAs and softmax must be done with it
+            if (!warp_wait(tc::smem_u32(&sm.q_empty), (qn & 1) ^ 1, abort_flag)) { ok = false; break; }
+            const uint16_t* qsrc = q_lat + (int64_t)i * H * D_LAT;
+            for (int c = lane; c < HP * 64; c += 32) {
+                const int row = c >> 6, u = c & 63;
+                const bool v = row < H;
+                tc::cp_async16(s_base + OFF_Q + (u >> 3) * Q_CHUNK + swz(row, u & 7),
+                               v ? (const void*)(qsrc + row * D_LAT + u * 8) : (const void*)q_lat, v);
+            }
+            tc::cp_async_commit();
+            tc::cp_async_wait<0>();
+            tc::fence_proxy_async();
+            __syncwarp();
+            if (lane == 0) {
+                sm.nb = nb;
+                tc::mbar_arrive(tc::smem_u32(&sm.q_full));
+            }
+            // latent-row blocks: lane l copies 16-byte units l and 32+l of every row of the block
+            for (int b = 0; b < nb; ++b, ++g) {
+                const int s = g % NSTAGE;
+                if (!warp_wait(tc::smem_u32(&sm.kv_empty[s]), ((g / NSTAGE) & 1) ^ 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t dst = s_base + OFF_KV + s * KV_BYTES;
+                int myv = -1;                     // this lane's slot: row `lane` of the block
+                {
+                    const int slot = b * BN + lane;
+                    const int v = slot < W ? irow[slot] : -1;
+                    myv = (v >= 0 && v < T) ? v : -1;
+                }
+                const uint32_t mask = __ballot_sync(0xffffffffu, myv >= 0);
 #pragma unroll 4
-            for (int kk = 0; kk < D_LAT / 16; ++kk) {
-                uint32_t a0, a1, a2, a3;
-                ldsm_x4(q_base + swz1k(mt * 16 + (lane & 15), kk * 2 + (lane >> 4)), a0, a1, a2, a3);
+                for (int r = 0; r < BN; ++r) {
+                    const int v = __shfl_sync(0xffffffffu, myv, r);
+                    const bool valid = v >= 0;
+                    const uint16_t* src = valid ? kv_lat + (int64_t)v * D_LAT : kv_lat;
 #pragma unroll
-                for (int pr = 0; pr < 2; ++pr) {
-                    const int nrow = half * 32 + pr * 16 + (lane & 7) + ((lane >> 4) << 3);
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4(kv_base[buf] + swz1k(nrow, kk * 2 + ((lane >> 3) & 1)), b0, b1, b2, b3);
-                    mma_bf16_16816(acc[pr * 2], a0, a1, a2, a3, b0, b1);
-                    mma_bf16_16816(acc[pr * 2 + 1], a0, a1, a2, a3, b2, b3);
+                    for (int k = 0; k < 2; ++k) {
+                        const int u = k * 32 + lane;          // one instruction = 512 contiguous bytes
+                        tc::cp_async16(dst + (u >> 3) * KV_CHUNK + swz(r, u & 7), src + (valid ? u * 8 : 0), valid);
+                    }
+                }
+                tc::cp_async_commit();
+                if (lane == 0) sm.mask[s] = mask;
+                if (b > 0) {
+                    // the previous block's copies are complete: publish it
+                    tc::cp_async_wait<1>();
+                    tc::fence_proxy_async();
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(tc::smem_u32(&sm.kv_full[(g - 1) % NSTAGE]));
                 }
             }
+            tc::cp_async_wait<0>();
+            tc::fence_proxy_async();
+            __syncwarp();
+            if (!ok) break;
+            if (lane == 0 && nb > 0) tc::mbar_arrive(tc::smem_u32(&sm.kv_full[(g - 1) % NSTAGE]));
+        }
+        tc::cp_async_wait<0>();
+        if (!ok) fail(sm, status);
+    } else if (warp == 2 || warp == 3) {
+        // ===================================================== MMA issuers
+        // warp 2: S half 0 (latent chunks 0-3) and every PV; warp 3: S half 1.
+        const int half = warp - 2;
+        if (lane == 0) {
+            uint32_t g = 0, qn = 0;
+            const uint32_t q_addr = s_base + OFF_Q;
+            auto pv = [&](uint32_t gg, int b) -> bool {
+                const int s = gg % NSTAGE, sb = gg % NSB;
+                if (!tc::mbar_wait(tc::smem_u32(&sm.p_full[sb]), (gg / NSB) & 1, abort_flag)) return false;
+                if (b == 0 && !tc::mbar_wait(tc::smem_u32(&sm.o_free), (qn & 1) ^ 1, abort_flag)) return false;
+                tc::fence_after();
+                const uint64_t a0 = tc::sw128_desc(s_base + OFF_KV + s * KV_BYTES, KV_CHUNK, 1024);
+                const uint64_t b0 = tc::sw128_desc(s_base + OFF_P + sb * P_BYTES, 0, 1024);
 #pragma unroll
-            for (int n = 0; n < 4; ++n) {
-                const int col = half * 32 + n * 8 + tig * 2;
-                const bool v0 = sm.idx[buf][col] >= 0, v1 = sm.idx[buf][col + 1] >= 0;
-                const int r0 = mt * 16 + g;
-                sm.s[r0 * S_STRIDE + col] = v0 ? acc[n][0] * scale_log2 : -INFINITY;
-                sm.s[r0 * S_STRIDE + col + 1] = v1 ? acc[n][1] * scale_log2 : -INFINITY;
-                sm.s[(r0 + 8) * S_STRIDE + col] = v0 ? acc[n][2] * scale_log2 : -INFINITY;
-                sm.s[(r0 + 8) * S_STRIDE + col + 1] = v1 ? acc[n][3] * scale_log2 : -INFINITY;
+                for (int kk = 0; kk < BN / 16; ++kk)
+#pragma unroll
+                    for (int t = 0; t < 4; ++t)
+                        tc::mma_bf16(tmem + TM_O + 64 * t, a0 + (uint64_t)(((2 * t) * KV_CHUNK + kk * 2048) >> 4),
+                                     b0 + (uint64_t)(kk * 2), ID_PV, (b == 0 && kk == 0) ? 0u : 1u);
+                tc::commit(tc::smem_u32(&sm.kv_empty[s]));
+                tc::commit(tc::smem_u32(&sm.p_empty[sb]));
+                tc::commit(tc::smem_u32(&sm.o_step[sb]));
+                return true;
+            };
+            bool ok = true;
+            for (int i = blockIdx.x; i < T && ok && !*abort_flag; i += gridDim.x, ++qn) {
+                if (!tc::mbar_wait(tc::smem_u32(&sm.q_full), qn & 1, abort_flag)) { ok = false; break; }
+                const int nb = sm.nb;
+                if (nb == 0) {
+                    tc::commit(tc::smem_u32(&sm.q_empty));
+                    if (half == 0) tc::commit(tc::smem_u32(&sm.o_full));
+                    continue;
+                }
+                for (int b = 0; b < nb; ++b, ++g) {
+                    const int s = g % NSTAGE, sb = g % NSB;
+                    if (!tc::mbar_wait(tc::smem_u32(&sm.kv_full[s]), (g / NSTAGE) & 1, abort_flag) ||
+                        !tc::mbar_wait(tc::smem_u32(&sm.s_free[sb]), ((g / NSB) & 1) ^ 1, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc::fence_after();
+                    const uint32_t kv = s_base + OFF_KV + s * KV_BYTES;
+                    const uint32_t d = tmem + TM_S + 64 * sb + 32 * half;
+                    // descriptors of K step 0 of this half; later steps only move the start address
+                    const uint64_t a0 = tc::sw128_desc(q_addr + half * 4 * Q_CHUNK, 0, 1024);
+                    const uint64_t b0 = tc::sw128_desc(kv + half * 4 * KV_CHUNK, 0, 1024);
+#pragma unroll
+                    for (int kl = 0; kl < D_LAT / 32; ++kl) {     // K steps of 16 latent columns
+                        tc::mma_bf16(d, a0 + (uint64_t)((kl >> 2) * (Q_CHUNK >> 4) + (kl & 3) * 2),
+                                     b0 + (uint64_t)((kl >> 2) * (KV_CHUNK >> 4) + (kl & 3) * 2), ID_S,
+                                     kl > 0 ? 1u : 0u);
+                    }
+                    tc::commit(tc::smem_u32(&sm.s_full[sb]));
+                    if (b == nb - 1) tc::commit(tc::smem_u32(&sm.q_empty));
+                    if (half == 1) {
+                        tc::commit(tc::smem_u32(&sm.kv_empty[s]));
+                    } else if (b > 0 && !pv(g - 1, b - 1)) {
+                        ok = false;
+                        break;
+                    }
+                }
+                if (!ok) break;
+                if (half == 0) {
+                    if (!pv(g - 1, nb - 1)) { ok = false; break; }
+                    tc::commit(tc::smem_u32(&sm.o_full));
+                }
+            }
+            if (!ok) fail(sm, status);
+            // drain every MMA this thread issued before TMEM is released
+            tc::commit(tc::smem_u32(&sm.drain));
+            const uint64_t t0 = tc::globaltimer_ns();
+            while (!tc::mbar_try(tc::smem_u32(&sm.drain), 0) && tc::globaltimer_ns() - t0 < tc::WAIT_LIMIT_NS) {
             }
         }
-        __syncthreads();
-
-        // ---- online softmax: 4 threads per head row, 16 slots each
-        {
-            const int row = tid >> 2, qtr = tid & 3;
-            if (row < MT * 16) {
-                float v[16];
+        __syncwarp();
+    } else if (warp >= 4) {
+        // ===================================================== softmax / correction / epilogue
+        // Row r = 16*wid + (lane & 15) (head), lane half hs = lane >> 4 owns the
+        // slot columns 16*hs .. 16*hs+15 of the block.  Stop decisions are
+        // taken together: `bad` is sticky per thread and is ORed across the
+        // four warps at every named barrier (bar.red.or).
+        const int wid = warp - 4;                   // TMEM subpartition
+        const int hs = lane >> 4;
+        const int h = wid * 16 + (lane & 15);       // head of this thread
+        const uint32_t lane_base = (uint32_t)(wid * 32) << 16;
+        uint32_t g = 0, qn = 0;
+        bool bad = false;
+        for (int i = blockIdx.x; i < T; i += gridDim.x, ++qn) {
+            bad = bad || !warp_wait(tc::smem_u32(&sm.q_full), qn & 1, abort_flag);
+            if (wg_or(bad)) { bad = true; break; }
+            const int nb = sm.nb;
+            wg_or(false);                           // every warp has read nb
+            if (tid == 128) tc::mbar_arrive(tc::smem_u32(&sm.q_empty));
+            float m_ref = -INFINITY, l = 0.f;       // m_ref equal in both lanes of a row; l partial
+            for (int b = 0; b < nb; ++b, ++g) {
+                const int s = g % NSTAGE, sb = g % NSB;
+                const int cb = g & 1;
+                float x[16];
+                bad = bad || !warp_wait(tc::smem_u32(&sm.s_full[sb]), (g / NSB) & 1, abort_flag);
+                if (!bad) {
+                    tc::fence_after();
+                    uint32_t va[32], vb[32];
+                    tc::tmem_ld32(tmem + lane_base + TM_S + 64 * sb, va);
+                    tc::tmem_ld32(tmem + lane_base + TM_S + 64 * sb + 32, vb);
+                    tc::tmem_wait_ld();
+                    tc::fence_before();
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(tc::smem_u32(&sm.s_free[sb]));
+                    // lanes 0-15 hold whole rows: hand the upper 16 columns to lane + 16
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float lo = __uint_as_float(va[j]) + __uint_as_float(vb[j]);
+                        const float hi = __uint_as_float(va[16 + j]) + __uint_as_float(vb[16 + j]);
+                        const float up = __shfl_sync(0xffffffffu, hi, lane & 15);
+                        x[j] = hs ? up : lo;
+                    }
+                    bad = !warp_wait(tc::smem_u32(&sm.kv_full[s]), (g / NSTAGE) & 1, abort_flag);
+                }
+                const uint32_t mask = bad ? 0u : (*reinterpret_cast<volatile uint32_t*>(&sm.mask[s]) >> (16 * hs));
                 float bmax = -INFINITY;
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
-                    v[j] = sm.s[row * S_STRIDE + qtr * 16 + j];
-                    bmax = fmaxf(bmax, v[j]);
+                    x[j] = ((mask >> j) & 1u) ? x[j] * scale_log2 : -INFINITY;
+                    bmax = fmaxf(bmax, x[j]);
                 }
-                bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, 1));
-                bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, 2));
-                const float m_old = sm.m[row];
-                const float m_new = fmaxf(m_old, bmax);
-                float alpha = 1.f, psum = 0.f;
-                uint32_t pk[8];
-                if (m_new == -INFINITY) {
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) pk[j] = 0u;
-                } else {
-                    alpha = exp2f(m_old - m_new);
-#pragma unroll
-                    for (int j = 0; j < 16; j += 2) {
-                        const float p0 = exp2f(v[j] - m_new), p1 = exp2f(v[j + 1] - m_new);
-                        psum += p0 + p1;
-                        pk[j >> 1] = pack_bf16(p0, p1);
+                bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, 16));
+                float alpha = 1.f;
+                bool need = false;
+                if (!bad) {
+                    if (m_ref == -INFINITY) {
+                        m_ref = bmax;                       // nothing accumulated for this head yet
+                    } else if (bmax > m_ref + TAU) {
+                        alpha = fast_exp2(m_ref - bmax);
+                        m_ref = bmax;
+                        l *= alpha;
+                        need = true;
                     }
                 }
-                psum += __shfl_xor_sync(0xffffffffu, psum, 1);
-                psum += __shfl_xor_sync(0xffffffffu, psum, 2);
-                *reinterpret_cast<uint4*>(sm.p + swz128(row, qtr * 2)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                *reinterpret_cast<uint4*>(sm.p + swz128(row, qtr * 2 + 1)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
-                if (qtr == 0) {
-                    sm.m[row] = m_new;
-                    sm.l[row] = sm.l[row] * alpha + psum;
-                    sm.alpha[row] = alpha;
+                if (hs == 0) sm.alpha[cb][h] = alpha;
+                if (wg_or(bad)) { bad = true; break; }
+                if (wg_or(need)) {
+                    // O^T must hold the previous block's PV before it is rescaled
+                    const uint32_t gp = g - 1;
+                    bad = !warp_wait(tc::smem_u32(&sm.o_step[gp % NSB]), (gp / NSB) & 1, abort_flag);
+                    if (!bad) {
+                        tc::fence_after();
+                        for (int t = 0; t < 4; ++t)
+                            for (int c0 = 0; c0 < HP; c0 += 32) {
+                                uint32_t o[32];
+                                const uint32_t ta = tmem + lane_base + TM_O + 64 * t + c0;
+                                tc::tmem_ld32(ta, o);
+                                tc::tmem_wait_ld();
+#pragma unroll
+                                for (int j = 0; j < 32; ++j)
+                                    o[j] = __float_as_uint(__uint_as_float(o[j]) * sm.alpha[cb][c0 + j]);
+                                tc::tmem_st32(ta, o);
+                            }
+                        tc::tmem_wait_st();
+                        tc::fence_before();
+                    }
+                }
+                // P^T row h, slots 16*hs .. 16*hs+15: 32 bytes, 16-byte units 2hs and 2hs+1
+                bad = bad || !warp_wait(tc::smem_u32(&sm.p_empty[sb]), ((g / NSB) & 1) ^ 1, abort_flag);
+                if (!bad) {
+                    uint32_t pk[8];
+                    float ps = 0.f;
+                    const bool live = m_ref != -INFINITY;
+#pragma unroll
+                    for (int j = 0; j < 16; j += 2) {
+                        const float p0 = live ? fast_exp2(x[j] - m_ref) : 0.f;
+                        const float p1 = live ? fast_exp2(x[j + 1] - m_ref) : 0.f;
+                        ps += p0 + p1;
+                        pk[j >> 1] = pack_bf16(p0, p1);
+                    }
+                    l += ps;
+                    uint8_t* prow = smem + OFF_P + sb * P_BYTES;
+                    *reinterpret_cast<uint4*>(prow + swz(h, 2 * hs)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    *reinterpret_cast<uint4*>(prow + swz(h, 2 * hs + 1)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+                    tc::fence_proxy_async();
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(tc::smem_u32(&sm.p_full[sb]));
                 }
             }
-        }
-        __syncthreads();
-
-        // ---- O = alpha * O + P V for 16 heads x 256 latent columns per warp
-        if (mt < MT) {
-            const float al0 = sm.alpha[mt * 16 + g], al1 = sm.alpha[mt * 16 + g + 8];
-#pragma unroll
-            for (int n = 0; n < 32; ++n) {
-                o[n][0] *= al0; o[n][1] *= al0;
-                o[n][2] *= al1; o[n][3] *= al1;
+            if (wg_or(bad)) { bad = true; break; }
+            // ---- epilogue: O^T / l -> bf16 out, lse
+            bad = !warp_wait(tc::smem_u32(&sm.o_full), qn & 1, abort_flag);
+            const float lt = l + __shfl_xor_sync(0xffffffffu, l, 16);
+            if (hs == 0) {
+                sm.inv_l[h] = lt > 0.f ? 1.f / lt : 0.f;
+                if (h < H)
+                    lse[(int64_t)i * H + h] = lt > 0.f ? (m_ref + log2f(lt)) * 0.69314718055994530942f : -INFINITY;
             }
+            if (wg_or(bad)) { bad = true; break; }
+            tc::fence_after();
+            uint16_t* orow = out + (int64_t)i * H * D_LAT;
+            uint8_t* stg = smem + OFF_STAGE + wid * (HP * 64);     // [64 heads][32 latent] bf16
+            for (int t = 0; t < 4; ++t) {
+                for (int c0 = 0; c0 < HP; c0 += 32) {
+                    uint32_t o[32];
+                    if (nb > 0) {
+                        tc::tmem_ld32(tmem + lane_base + TM_O + 64 * t + c0, o);
+                        tc::tmem_wait_ld();
+                    } else {
 #pragma unroll
-            for (int kk = 0; kk < BN / 16; ++kk) {
-                uint32_t a0, a1, a2, a3;
-                ldsm_x4(p_base + swz128(mt * 16 + (lane & 15), kk * 2 + (lane >> 4)), a0, a1, a2, a3);
-                const int krow = kk * 16 + (lane & 7) + (((lane >> 3) & 1) << 3);
+                        for (int j = 0; j < 32; ++j) o[j] = 0u;
+                    }
 #pragma unroll
-                for (int np = 0; np < 16; ++np) {
-                    const int chunk = (half * 256 + np * 16) / 8 + (lane >> 4);
-                    uint32_t b0, b1, b2, b3;
-                    ldsm_x4_t(kv_base[buf] + swz1k(krow, chunk), b0, b1, b2, b3);
-                    mma_bf16_16816(o[np * 2], a0, a1, a2, a3, b0, b1);
-                    mma_bf16_16816(o[np * 2 + 1], a0, a1, a2, a3, b2, b3);
+                    for (int j = 0; j < 32; ++j) {
+                        const float val = __uint_as_float(o[j]) * sm.inv_l[c0 + j];
+                        reinterpret_cast<__nv_bfloat16*>(stg + (c0 + j) * 64)[lane] = __float2bfloat16_rn(val);
+                    }
                 }
-            }
-        }
-        __syncthreads();
-    }
-
-    // ---- epilogue: normalise, round to bf16, write out and lse
-    if (mt < MT) {
-        const int r0 = mt * 16 + g, r1 = r0 + 8;
-        const float l0 = sm.l[r0], l1 = sm.l[r1];
-        const float inv0 = l0 > 0.f ? 1.f / l0 : 0.f, inv1 = l1 > 0.f ? 1.f / l1 : 0.f;
+                __syncwarp();
+                // 64 heads x 64 B: 16-byte stores, 8 per lane
 #pragma unroll
-        for (int n = 0; n < 32; ++n) {
-            const int col = half * 256 + n * 8 + tig * 2;
-            if (r0 < H)
-                *reinterpret_cast<uint32_t*>(out + ((int64_t)i * H + r0) * D_LAT + col) =
-                    pack_bf16(o[n][0] * inv0, o[n][1] * inv0);
-            if (r1 < H)
-                *reinterpret_cast<uint32_t*>(out + ((int64_t)i * H + r1) * D_LAT + col) =
-                    pack_bf16(o[n][2] * inv1, o[n][3] * inv1);
+                for (int k = 0; k < 8; ++k) {
+                    const int cidx = k * 32 + lane;        // 0..255
+                    const int hh = cidx >> 2, part = cidx & 3;
+                    if (hh < H) {
+                        const uint4 val = *reinterpret_cast<const uint4*>(stg + hh * 64 + part * 16);
+                        *reinterpret_cast<uint4*>(orow + hh * D_LAT + t * 128 + wid * 32 + part * 8) = val;
+                    }
+                }
+                __syncwarp();
+            }
+            tc::fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(tc::smem_u32(&sm.o_free));
+            wg_or(false);                           // inv_l is rewritten by the next query
         }
+        if (bad) fail(sm, status);
     }
-    if (tid < H) {
-        const float l = sm.l[tid];
-        lse[(int64_t)i * H + tid] = l > 0.f ? (sm.m[tid] + log2f(l)) * 0.69314718055994530942f : -INFINITY;
+    tc::fence_before();
+    __syncthreads();
+    if (warp == 2) {
+        tc::fence_after();
+        tc::tmem_dealloc(tmem, TM_COLS);
     }
-}
-
-template <int MT>
-static int launch_mla_t(const uint16_t* q_lat, const uint16_t* kv_lat, const int32_t* indices, int W, int T, int H,
-                        float scale, uint16_t* out, float* lse, int32_t* status, cudaStream_t stream) {
-    const int smem = (int)sizeof(MlaSmem);
-    static bool attr_done[64] = {false};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev >= 0 && dev < 64 && !attr_done[dev]) {
-        if (cudaFuncSetAttribute(sparse_mla_kernel<MT>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-            cudaSuccess)
-            return KPOOL_ERR_CUDA;
-        attr_done[dev] = true;
-    }
-    const float scale_log2 = scale * 1.4426950408889634f;
-    sparse_mla_kernel<MT><<<T, MLA_THREADS, smem, stream>>>(q_lat, kv_lat, indices, W, T, H, scale_log2, out, lse,
-                                                            status);
-    return cudaGetLastError() == cudaSuccess ? KPOOL_OK : KPOOL_ERR_CUDA;
 }
 
 int launch_sparse_mla(const uint16_t* q_lat, const uint16_t* kv_lat, const int32_t* indices, int W, int T,
                       int n_heads, float scale, uint16_t* out, float* lse, int32_t* status, cudaStream_t stream) {
     if (T <= 0) return KPOOL_OK;
-    switch ((n_heads + 15) / 16) {
-        case 1: return launch_mla_t<1>(q_lat, kv_lat, indices, W, T, n_heads, scale, out, lse, status, stream);
-        case 2: return launch_mla_t<2>(q_lat, kv_lat, indices, W, T, n_heads, scale, out, lse, status, stream);
-        case 3: return launch_mla_t<3>(q_lat, kv_lat, indices, W, T, n_heads, scale, out, lse, status, stream);
-        case 4: return launch_mla_t<4>(q_lat, kv_lat, indices, W, T, n_heads, scale, out, lse, status, stream);
-        default: return KPOOL_ERR_SHAPE;
+    if (n_heads < 1 || n_heads > HP) return KPOOL_ERR_SHAPE;
+    static int n_sm[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return KPOOL_ERR_CUDA;
+    if (n_sm[dev] == 0) {
+        if (cudaFuncSetAttribute(sparse_mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
+            cudaSuccess)
+            return KPOOL_ERR_CUDA;
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return KPOOL_ERR_CUDA;
+        n_sm[dev] = sms;
     }
+    const int grid = T < n_sm[dev] ? T : n_sm[dev];
+    const float scale_log2 = scale * 1.4426950408889634f;
+    sparse_mla_tc_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(q_lat, kv_lat, indices, W, T, n_heads, scale_log2,
+                                                               out, lse, status);
+    return cudaGetLastError() == cudaSuccess ? KPOOL_OK : KPOOL_ERR_CUDA;
 }
 
 }  // namespace kpool
