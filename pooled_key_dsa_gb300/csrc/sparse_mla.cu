@@ -8,27 +8,36 @@
 //
 // Persistent CTAs (one per SM), each walking query tokens i = blockIdx.x +
 // k*gridDim.x.  For one query the index row is cut into blocks of 32 slots:
-//   S   = Q Kv^T      tcgen05 kind::f16, M = 64 heads, N = 32 slots, K = 512
+//   S   = Q Kv^T      tcgen05 kind::f16, M = 64 heads, N = 32 slots, K = 512,
+//                     split over two issuing warps (latent 0-255 / 256-511,
+//                     two accumulators the softmax adds)
 //   O^T += Kv^T P^T   tcgen05 kind::f16, M = 128 latent rows (4 tiles),
 //                     N = 64 heads, K = 32 slots; A is the gathered block read
 //                     MN-major, so the tile that fed S also feeds PV
 // Q (64 KB) stays in shared memory for the whole query; gathered latent rows
-// go through a 4-stage ring of 32 KB blocks; S (2 x 32 columns) and O^T
-// (4 x 64 columns) live in TMEM.
+// go through a 4-stage ring of 32 KB blocks; S (2 buffers x 2 halves x 32
+// columns) and O^T (4 x 64 columns) live in TMEM.
 //
-// Warp roles (256 threads):
-//   warp 0     producer: index scan, Q and latent-row gathers (cp.async 16 B,
-//              128-byte swizzle written by hand), mbarrier hand-off
-//   warp 2     TMEM owner; lane 0 issues S over latent 0..255 and every PV
-//   warp 3     lane 0 issues S over latent 256..511 into a second
-//              accumulator (one thread cannot issue MMAs fast enough for
-//              these small shapes); the softmax adds the two halves
+// The latent gather from L2 is this kernel's binding resource (about 1 KB per
+// slot, shared by nothing across queries), so four producer warps keep many
+// 16-byte cp.async in flight; each lane's copies arrive on the stage's
+// mbarrier when they land (cp.async.mbarrier.arrive.noinc), so no producer
+// ever waits for a copy, and the MMA issuers take a proxy fence before
+// reading the tile.
+//
+// Warp roles (384 threads):
+//   warps 0-3  producers: index scan, Q, latent rows (128-byte swizzle
+//              written by hand), 8 rows of every block per warp
 //   warps 4-7  softmax: the M=64 accumulator sits in lanes 0-15 of each
 //              warp's TMEM subpartition; after the load, lanes 16-31 take the
-//              upper half of every row's slots, so all 32 lanes work.  Lazy
-//              rescale of O^T only when a head's running max grows by more
-//              than 2^8; P^T to shared memory in the operand layout; epilogue
-//              O^T / l -> bf16
+//              upper 16 slots of every row, so all 32 lanes work.  The running
+//              max only moves (and O^T is rescaled) when a slot beats it by
+//              more than 2^8; a vote on that is the only barrier of a block in
+//              the common case.  P^T goes to shared memory in the operand
+//              layout; the epilogue writes O^T / l as bf16 through a staging
+//              tile (the P buffers, idle by then).
+//   warps 8-9  S issuers (warp 8 also owns the TMEM allocation)
+//   warp 10    PV issuer
 // Every wait is bounded and warp-uniform (lane 0 polls, the warp takes its
 // answer); on expiry the kernel records KPOOL_ERR_TIMEOUT, the softmax warps
 // agree on stopping at their next named barrier, every role leaves its loop,
@@ -48,26 +57,25 @@ constexpr int NSTAGE = 4;              // latent-row ring depth
 constexpr int NSB = 2;                 // S / P double buffers
 constexpr int HP = 64;                 // head rows (M of S, N of PV)
 constexpr float TAU = 8.0f;            // lazy-rescale threshold (log2 units)
-constexpr int THREADS = 256;
+constexpr int THREADS = 384;
+constexpr int NPROD = 4;               // producer warps
 
 constexpr int Q_BYTES = HP * D_LAT * 2;          // 64 KB: 8 chunks x [64 rows x 128 B]
 constexpr int Q_CHUNK = HP * 128;                // 8 KB
 constexpr int KV_BYTES = BN * D_LAT * 2;         // 32 KB: 8 chunks x [32 rows x 128 B]
 constexpr int KV_CHUNK = BN * 128;               // 4 KB
-constexpr int P_BYTES = HP * 128;                // 8 KB: [64 head rows x 128 B] (first 64 B used)
-constexpr int STAGE_BYTES = 4 * HP * 64;         // 16 KB epilogue staging (4 warps x 64 heads x 32 bf16)
+constexpr int P_BYTES = HP * 128;                // 8 KB: [64 head rows x 128 B], first 64 B used
 
 constexpr int OFF_Q = 0;
 constexpr int OFF_KV = OFF_Q + Q_BYTES;
-constexpr int OFF_P = OFF_KV + NSTAGE * KV_BYTES;
-constexpr int OFF_STAGE = OFF_P + NSB * P_BYTES;
-constexpr int OFF_SMALL = OFF_STAGE + STAGE_BYTES;
+constexpr int OFF_P = OFF_KV + NSTAGE * KV_BYTES;        // 2 P buffers = the 16 KB epilogue staging
+constexpr int OFF_SMALL = OFF_P + NSB * P_BYTES;
 
 struct Small {
     uint64_t q_full, q_empty, o_full, o_free, drain;
     uint64_t kv_full[NSTAGE], kv_empty[NSTAGE];
     uint64_t s_full[NSB], s_free[NSB], p_full[NSB], p_empty[NSB], o_step[NSB];
-    uint32_t mask[NSTAGE];
+    uint8_t mask[NSTAGE][NPROD];           // valid-slot bits, 8 slots per producer warp
     int nb;
     int abort;
     uint32_t tmem;
@@ -77,7 +85,7 @@ struct Small {
 constexpr int SMEM_BYTES = OFF_SMALL + (int)sizeof(Small) + 1024;   // + alignment slack
 
 constexpr uint32_t TM_O = 0;           // O^T tile t at columns 64t
-constexpr uint32_t TM_S = 256;         // S buffer b, half k (latent 256k..256k+255) at 256 + 64b + 32k
+constexpr uint32_t TM_S = 256;         // S buffer b, latent half k at 256 + 64b + 32k
 constexpr uint32_t TM_COLS = 512;
 
 constexpr uint32_t ID_S = tc::idesc(64, BN, 1, 1, false, false);
@@ -137,17 +145,17 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
     volatile int* abort_flag = &sm.abort;
 
     if (tid == 0) {
-        tc::mbar_init(tc::smem_u32(&sm.q_full), 1);
-        tc::mbar_init(tc::smem_u32(&sm.q_empty), 3);      // two MMA issuers + softmax acknowledgement
+        tc::mbar_init(tc::smem_u32(&sm.q_full), NPROD * 32 + 1);      // every producer lane's copies + nb
+        tc::mbar_init(tc::smem_u32(&sm.q_empty), 4);      // two S issuers, PV issuer, softmax
         tc::mbar_init(tc::smem_u32(&sm.o_full), 1);
         tc::mbar_init(tc::smem_u32(&sm.o_free), 4);
-        tc::mbar_init(tc::smem_u32(&sm.drain), 2);
+        tc::mbar_init(tc::smem_u32(&sm.drain), 3);
         for (int s = 0; s < NSTAGE; ++s) {
-            tc::mbar_init(tc::smem_u32(&sm.kv_full[s]), 1);
-            tc::mbar_init(tc::smem_u32(&sm.kv_empty[s]), 2);    // S-half issuer + PV issuer
+            tc::mbar_init(tc::smem_u32(&sm.kv_full[s]), NPROD * 32 + NPROD);   // copies + masks
+            tc::mbar_init(tc::smem_u32(&sm.kv_empty[s]), 3);   // two S issuers + PV issuer
         }
         for (int b = 0; b < NSB; ++b) {
-            tc::mbar_init(tc::smem_u32(&sm.s_full[b]), 2);      // both halves of S
+            tc::mbar_init(tc::smem_u32(&sm.s_full[b]), 2);     // both halves of S
             tc::mbar_init(tc::smem_u32(&sm.s_free[b]), 4);
             tc::mbar_init(tc::smem_u32(&sm.p_full[b]), 4);
             tc::mbar_init(tc::smem_u32(&sm.p_empty[b]), 1);
@@ -156,14 +164,16 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
         sm.abort = 0;
         tc::mbar_init_fence();
     }
-    if (warp == 2) tc::tmem_alloc(tc::smem_u32(&sm.tmem), TM_COLS);
+    if (warp == 8) tc::tmem_alloc(tc::smem_u32(&sm.tmem), TM_COLS);
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
     const uint32_t tmem = sm.tmem;
 
-    if (warp == 0) {
-        // ===================================================== producer (one warp)
+    if (warp < NPROD) {
+        // ===================================================== producers
+        // Warp w copies Q rows 16w..16w+15 and rows 8w..8w+7 of every block;
+        // lane l copies 16-byte units l and 32+l of a row.
         uint32_t g = 0;                             // global block counter
         uint32_t qn = 0;
         bool ok = true;
@@ -175,105 +185,80 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
             for (int j = lane; j < W; j += 32) {
                 const int v = irow[j];
                 if (v >= 0 && v < T) last = j;
-                else if (v != -1) set_status(status, KPOOL_ERR_INDEX_RANGE);
+                else if (v != -1 && warp == 0) set_status(status, KPOOL_ERR_INDEX_RANGE);
             }
             for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
             const int nb = (last + BN) / BN;
-            // Q tile: the previous query's S MMAs and softmax must be done with it
+            // Q tile: the previous query's S MMAs and every reader of nb must be done
             if (!warp_wait(tc::smem_u32(&sm.q_empty), (qn & 1) ^ 1, abort_flag)) { ok = false; break; }
             const uint16_t* qsrc = q_lat + (int64_t)i * H * D_LAT;
-            for (int c = lane; c < HP * 64; c += 32) {
-                const int row = c >> 6, u = c & 63;
+#pragma unroll 2
+            for (int rr = 0; rr < HP / NPROD; ++rr) {
+                const int row = warp * (HP / NPROD) + rr;
                 const bool v = row < H;
-                tc::cp_async16(s_base + OFF_Q + (u >> 3) * Q_CHUNK + swz(row, u & 7),
-                               v ? (const void*)(qsrc + row * D_LAT + u * 8) : (const void*)q_lat, v);
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const int u = k * 32 + lane;
+                    tc::cp_async16(s_base + OFF_Q + (u >> 3) * Q_CHUNK + swz(row, u & 7),
+                                   v ? (const void*)(qsrc + row * D_LAT + u * 8) : (const void*)q_lat, v);
+                }
             }
-            tc::cp_async_commit();
-            tc::cp_async_wait<0>();
-            tc::fence_proxy_async();
-            __syncwarp();
-            if (lane == 0) {
+            tc::cp_async_arrive_noinc(tc::smem_u32(&sm.q_full));
+            if (warp == 0 && lane == 0) {
                 sm.nb = nb;
                 tc::mbar_arrive(tc::smem_u32(&sm.q_full));
             }
-            // latent-row blocks: lane l copies 16-byte units l and 32+l of every row of the block
             for (int b = 0; b < nb; ++b, ++g) {
                 const int s = g % NSTAGE;
                 if (!warp_wait(tc::smem_u32(&sm.kv_empty[s]), ((g / NSTAGE) & 1) ^ 1, abort_flag)) {
                     ok = false;
                     break;
                 }
-                const uint32_t dst = s_base + OFF_KV + s * KV_BYTES;
-                int myv = -1;                     // this lane's slot: row `lane` of the block
-                {
-                    const int slot = b * BN + lane;
+                int myv = -1;                       // lane l < 8: slot 8w + l of the block
+                if (lane < 8) {
+                    const int slot = b * BN + warp * 8 + lane;
                     const int v = slot < W ? irow[slot] : -1;
                     myv = (v >= 0 && v < T) ? v : -1;
                 }
-                const uint32_t mask = __ballot_sync(0xffffffffu, myv >= 0);
-#pragma unroll 4
-                for (int r = 0; r < BN; ++r) {
-                    const int v = __shfl_sync(0xffffffffu, myv, r);
+                const uint32_t m8 = __ballot_sync(0xffffffffu, myv >= 0) & 0xffu;
+                const uint32_t dst = s_base + OFF_KV + s * KV_BYTES;
+#pragma unroll
+                for (int rr = 0; rr < 8; ++rr) {
+                    const int row = warp * 8 + rr;
+                    const int v = __shfl_sync(0xffffffffu, myv, rr);
                     const bool valid = v >= 0;
                     const uint16_t* src = valid ? kv_lat + (int64_t)v * D_LAT : kv_lat;
 #pragma unroll
                     for (int k = 0; k < 2; ++k) {
                         const int u = k * 32 + lane;          // one instruction = 512 contiguous bytes
-                        tc::cp_async16(dst + (u >> 3) * KV_CHUNK + swz(r, u & 7), src + (valid ? u * 8 : 0), valid);
+                        tc::cp_async16(dst + (u >> 3) * KV_CHUNK + swz(row, u & 7), src + (valid ? u * 8 : 0), valid);
                     }
                 }
-                tc::cp_async_commit();
-                if (lane == 0) sm.mask[s] = mask;
-                if (b > 0) {
-                    // the previous block's copies are complete: publish it
-                    tc::cp_async_wait<1>();
-                    tc::fence_proxy_async();
-                    __syncwarp();
-                    if (lane == 0) tc::mbar_arrive(tc::smem_u32(&sm.kv_full[(g - 1) % NSTAGE]));
+                tc::cp_async_arrive_noinc(tc::smem_u32(&sm.kv_full[s]));
+                if (lane == 0) {
+                    sm.mask[s][warp] = (uint8_t)m8;
+                    tc::mbar_arrive(tc::smem_u32(&sm.kv_full[s]));
                 }
             }
-            tc::cp_async_wait<0>();
-            tc::fence_proxy_async();
-            __syncwarp();
-            if (!ok) break;
-            if (lane == 0 && nb > 0) tc::mbar_arrive(tc::smem_u32(&sm.kv_full[(g - 1) % NSTAGE]));
         }
         tc::cp_async_wait<0>();
         if (!ok) fail(sm, status);
-    } else if (warp == 2 || warp == 3) {
-        // ===================================================== MMA issuers
-        // warp 2: S half 0 (latent chunks 0-3) and every PV; warp 3: S half 1.
-        const int half = warp - 2;
+    } else if (warp == 8 || warp == 9) {
+        // ===================================================== S issuers (latent half = warp - 8)
+        const int half = warp - 8;
         if (lane == 0) {
             uint32_t g = 0, qn = 0;
             const uint32_t q_addr = s_base + OFF_Q;
-            auto pv = [&](uint32_t gg, int b) -> bool {
-                const int s = gg % NSTAGE, sb = gg % NSB;
-                if (!tc::mbar_wait(tc::smem_u32(&sm.p_full[sb]), (gg / NSB) & 1, abort_flag)) return false;
-                if (b == 0 && !tc::mbar_wait(tc::smem_u32(&sm.o_free), (qn & 1) ^ 1, abort_flag)) return false;
-                tc::fence_after();
-                const uint64_t a0 = tc::sw128_desc(s_base + OFF_KV + s * KV_BYTES, KV_CHUNK, 1024);
-                const uint64_t b0 = tc::sw128_desc(s_base + OFF_P + sb * P_BYTES, 0, 1024);
-#pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk)
-#pragma unroll
-                    for (int t = 0; t < 4; ++t)
-                        tc::mma_bf16(tmem + TM_O + 64 * t, a0 + (uint64_t)(((2 * t) * KV_CHUNK + kk * 2048) >> 4),
-                                     b0 + (uint64_t)(kk * 2), ID_PV, (b == 0 && kk == 0) ? 0u : 1u);
-                tc::commit(tc::smem_u32(&sm.kv_empty[s]));
-                tc::commit(tc::smem_u32(&sm.p_empty[sb]));
-                tc::commit(tc::smem_u32(&sm.o_step[sb]));
-                return true;
-            };
             bool ok = true;
             for (int i = blockIdx.x; i < T && ok && !*abort_flag; i += gridDim.x, ++qn) {
                 if (!tc::mbar_wait(tc::smem_u32(&sm.q_full), qn & 1, abort_flag)) { ok = false; break; }
+                tc::fence_proxy_async();                // Q was written by cp.async (generic proxy)
                 const int nb = sm.nb;
                 if (nb == 0) {
                     tc::commit(tc::smem_u32(&sm.q_empty));
-                    if (half == 0) tc::commit(tc::smem_u32(&sm.o_full));
                     continue;
                 }
+                const uint64_t a0 = tc::sw128_desc(q_addr + half * 4 * Q_CHUNK, 0, 1024);
                 for (int b = 0; b < nb; ++b, ++g) {
                     const int s = g % NSTAGE, sb = g % NSB;
                     if (!tc::mbar_wait(tc::smem_u32(&sm.kv_full[s]), (g / NSTAGE) & 1, abort_flag) ||
@@ -281,47 +266,73 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
                         ok = false;
                         break;
                     }
+                    tc::fence_proxy_async();            // the block was written by cp.async
                     tc::fence_after();
-                    const uint32_t kv = s_base + OFF_KV + s * KV_BYTES;
+                    const uint64_t b0 = tc::sw128_desc(s_base + OFF_KV + s * KV_BYTES + half * 4 * KV_CHUNK, 0, 1024);
                     const uint32_t d = tmem + TM_S + 64 * sb + 32 * half;
-                    // descriptors of K step 0 of this half; later steps only move the start address
-                    const uint64_t a0 = tc::sw128_desc(q_addr + half * 4 * Q_CHUNK, 0, 1024);
-                    const uint64_t b0 = tc::sw128_desc(kv + half * 4 * KV_CHUNK, 0, 1024);
 #pragma unroll
-                    for (int kl = 0; kl < D_LAT / 32; ++kl) {     // K steps of 16 latent columns
+                    for (int kl = 0; kl < D_LAT / 32; ++kl)      // K steps of 16 latent columns
                         tc::mma_bf16(d, a0 + (uint64_t)((kl >> 2) * (Q_CHUNK >> 4) + (kl & 3) * 2),
                                      b0 + (uint64_t)((kl >> 2) * (KV_CHUNK >> 4) + (kl & 3) * 2), ID_S,
                                      kl > 0 ? 1u : 0u);
-                    }
                     tc::commit(tc::smem_u32(&sm.s_full[sb]));
+                    tc::commit(tc::smem_u32(&sm.kv_empty[s]));
                     if (b == nb - 1) tc::commit(tc::smem_u32(&sm.q_empty));
-                    if (half == 1) {
-                        tc::commit(tc::smem_u32(&sm.kv_empty[s]));
-                    } else if (b > 0 && !pv(g - 1, b - 1)) {
-                        ok = false;
-                        break;
-                    }
-                }
-                if (!ok) break;
-                if (half == 0) {
-                    if (!pv(g - 1, nb - 1)) { ok = false; break; }
-                    tc::commit(tc::smem_u32(&sm.o_full));
                 }
             }
             if (!ok) fail(sm, status);
-            // drain every MMA this thread issued before TMEM is released
             tc::commit(tc::smem_u32(&sm.drain));
             const uint64_t t0 = tc::globaltimer_ns();
             while (!tc::mbar_try(tc::smem_u32(&sm.drain), 0) && tc::globaltimer_ns() - t0 < tc::WAIT_LIMIT_NS) {
             }
         }
         __syncwarp();
-    } else if (warp >= 4) {
+    } else if (warp == 10) {
+        // ===================================================== PV issuer
+        if (lane == 0) {
+            uint32_t g = 0, qn = 0;
+            bool ok = true;
+            for (int i = blockIdx.x; i < T && ok && !*abort_flag; i += gridDim.x, ++qn) {
+                if (!tc::mbar_wait(tc::smem_u32(&sm.q_full), qn & 1, abort_flag)) { ok = false; break; }
+                const int nb = sm.nb;
+                tc::mbar_arrive(tc::smem_u32(&sm.q_empty));   // nb has been read
+                for (int b = 0; b < nb; ++b, ++g) {
+                    const int s = g % NSTAGE, sb = g % NSB;
+                    if (!tc::mbar_wait(tc::smem_u32(&sm.p_full[sb]), (g / NSB) & 1, abort_flag) ||
+                        (b == 0 && !tc::mbar_wait(tc::smem_u32(&sm.o_free), (qn & 1) ^ 1, abort_flag))) {
+                        ok = false;
+                        break;
+                    }
+                    tc::fence_proxy_async();
+                    tc::fence_after();
+                    const uint64_t a0 = tc::sw128_desc(s_base + OFF_KV + s * KV_BYTES, KV_CHUNK, 1024);
+                    const uint64_t b0 = tc::sw128_desc(s_base + OFF_P + sb * P_BYTES, 0, 1024);
+#pragma unroll
+                    for (int kk = 0; kk < BN / 16; ++kk)
+#pragma unroll
+                        for (int t = 0; t < 4; ++t)
+                            tc::mma_bf16(tmem + TM_O + 64 * t,
+                                         a0 + (uint64_t)(((2 * t) * KV_CHUNK + kk * 2048) >> 4),
+                                         b0 + (uint64_t)(kk * 2), ID_PV, (b == 0 && kk == 0) ? 0u : 1u);
+                    tc::commit(tc::smem_u32(&sm.kv_empty[s]));
+                    tc::commit(tc::smem_u32(&sm.p_empty[sb]));
+                    tc::commit(tc::smem_u32(&sm.o_step[sb]));
+                }
+                if (!ok) break;
+                tc::commit(tc::smem_u32(&sm.o_full));      // once per query, also for an empty row
+            }
+            if (!ok) fail(sm, status);
+            tc::commit(tc::smem_u32(&sm.drain));
+            const uint64_t t0 = tc::globaltimer_ns();
+            while (!tc::mbar_try(tc::smem_u32(&sm.drain), 0) && tc::globaltimer_ns() - t0 < tc::WAIT_LIMIT_NS) {
+            }
+        }
+        __syncwarp();
+    } else if (warp >= 4 && warp < 8) {
         // ===================================================== softmax / correction / epilogue
-        // Row r = 16*wid + (lane & 15) (head), lane half hs = lane >> 4 owns the
-        // slot columns 16*hs .. 16*hs+15 of the block.  Stop decisions are
-        // taken together: `bad` is sticky per thread and is ORed across the
-        // four warps at every named barrier (bar.red.or).
+        // Row h = 16*wid + (lane & 15) (head); lane half hs = lane >> 4 owns
+        // slots 16*hs .. 16*hs+15 of the block.  `bad` is sticky per thread and
+        // ORed across the four warps at every named barrier (bar.red.or).
         const int wid = warp - 4;                   // TMEM subpartition
         const int hs = lane >> 4;
         const int h = wid * 16 + (lane & 15);       // head of this thread
@@ -342,14 +353,11 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
                 bad = bad || !warp_wait(tc::smem_u32(&sm.s_full[sb]), (g / NSB) & 1, abort_flag);
                 if (!bad) {
                     tc::fence_after();
+                    // lanes 0-15 hold whole rows: keep slots 0-15, hand slots 16-31 to lane + 16
                     uint32_t va[32], vb[32];
                     tc::tmem_ld32(tmem + lane_base + TM_S + 64 * sb, va);
                     tc::tmem_ld32(tmem + lane_base + TM_S + 64 * sb + 32, vb);
                     tc::tmem_wait_ld();
-                    tc::fence_before();
-                    __syncwarp();
-                    if (lane == 0) tc::mbar_arrive(tc::smem_u32(&sm.s_free[sb]));
-                    // lanes 0-15 hold whole rows: hand the upper 16 columns to lane + 16
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const float lo = __uint_as_float(va[j]) + __uint_as_float(vb[j]);
@@ -357,52 +365,61 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
                         const float up = __shfl_sync(0xffffffffu, hi, lane & 15);
                         x[j] = hs ? up : lo;
                     }
+                    tc::fence_before();
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(tc::smem_u32(&sm.s_free[sb]));
                     bad = !warp_wait(tc::smem_u32(&sm.kv_full[s]), (g / NSTAGE) & 1, abort_flag);
                 }
-                const uint32_t mask = bad ? 0u : (*reinterpret_cast<volatile uint32_t*>(&sm.mask[s]) >> (16 * hs));
-                float bmax = -INFINITY;
+                const uint32_t mask =
+                    bad ? 0u : ((*reinterpret_cast<volatile uint32_t*>(&sm.mask[s][0]) >> (16 * hs)) & 0xffffu);
+                const float thr = m_ref + TAU;        // -inf for a row that has seen no valid slot yet
+                bool exceed = false;
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
                     x[j] = ((mask >> j) & 1u) ? x[j] * scale_log2 : -INFINITY;
-                    bmax = fmaxf(bmax, x[j]);
+                    exceed |= x[j] > thr;
                 }
-                bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, 16));
-                float alpha = 1.f;
-                bool need = false;
-                if (!bad) {
-                    if (m_ref == -INFINITY) {
-                        m_ref = bmax;                       // nothing accumulated for this head yet
-                    } else if (bmax > m_ref + TAU) {
-                        alpha = fast_exp2(m_ref - bmax);
-                        m_ref = bmax;
-                        l *= alpha;
-                        need = true;
-                    }
-                }
-                if (hs == 0) sm.alpha[cb][h] = alpha;
-                if (wg_or(bad)) { bad = true; break; }
-                if (wg_or(need)) {
-                    // O^T must hold the previous block's PV before it is rescaled
-                    const uint32_t gp = g - 1;
-                    bad = !warp_wait(tc::smem_u32(&sm.o_step[gp % NSB]), (gp / NSB) & 1, abort_flag);
-                    if (!bad) {
-                        tc::fence_after();
-                        for (int t = 0; t < 4; ++t)
-                            for (int c0 = 0; c0 < HP; c0 += 32) {
-                                uint32_t o[32];
-                                const uint32_t ta = tmem + lane_base + TM_O + 64 * t + c0;
-                                tc::tmem_ld32(ta, o);
-                                tc::tmem_wait_ld();
+                // common case: no running max moves, one barrier per block
+                if (wg_or(bad || exceed)) {
+                    if (wg_or(bad)) { bad = true; break; }
+                    float bmax = -INFINITY;
 #pragma unroll
-                                for (int j = 0; j < 32; ++j)
-                                    o[j] = __float_as_uint(__uint_as_float(o[j]) * sm.alpha[cb][c0 + j]);
-                                tc::tmem_st32(ta, o);
-                            }
-                        tc::tmem_wait_st();
-                        tc::fence_before();
+                    for (int j = 0; j < 16; ++j) bmax = fmaxf(bmax, x[j]);
+                    bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, 16));
+                    float alpha = 1.f;
+                    bool need = false;
+                    if (bmax > m_ref + TAU) {
+                        if (m_ref != -INFINITY) {          // O^T holds this head's earlier slots
+                            alpha = fast_exp2(m_ref - bmax);
+                            l *= alpha;
+                            need = true;
+                        }
+                        m_ref = bmax;
+                    }
+                    if (hs == 0) sm.alpha[cb][h] = alpha;
+                    if (wg_or(need)) {
+                        // O^T must hold the previous block's PV before it is rescaled
+                        const uint32_t gp = g - 1;
+                        bad = !warp_wait(tc::smem_u32(&sm.o_step[gp % NSB]), (gp / NSB) & 1, abort_flag);
+                        if (!bad) {
+                            tc::fence_after();
+                            for (int t = 0; t < 4; ++t)
+                                for (int c0 = 0; c0 < HP; c0 += 32) {
+                                    uint32_t o[32];
+                                    const uint32_t ta = tmem + lane_base + TM_O + 64 * t + c0;
+                                    tc::tmem_ld32(ta, o);
+                                    tc::tmem_wait_ld();
+#pragma unroll
+                                    for (int j = 0; j < 32; ++j)
+                                        o[j] = __float_as_uint(__uint_as_float(o[j]) * sm.alpha[cb][c0 + j]);
+                                    tc::tmem_st32(ta, o);
+                                }
+                            tc::tmem_wait_st();
+                            tc::fence_before();
+                        }
                     }
                 }
-                // P^T row h, slots 16*hs .. 16*hs+15: 32 bytes, 16-byte units 2hs and 2hs+1
+                // P^T row h, slots 16*hs .. 16*hs+15: 32 bytes, 16-byte units 2hs, 2hs+1
                 bad = bad || !warp_wait(tc::smem_u32(&sm.p_empty[sb]), ((g / NSB) & 1) ^ 1, abort_flag);
                 if (!bad) {
                     uint32_t pk[8];
@@ -436,7 +453,7 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
             if (wg_or(bad)) { bad = true; break; }
             tc::fence_after();
             uint16_t* orow = out + (int64_t)i * H * D_LAT;
-            uint8_t* stg = smem + OFF_STAGE + wid * (HP * 64);     // [64 heads][32 latent] bf16
+            uint8_t* stg = smem + OFF_P + wid * (HP * 64);        // [64 heads][32 latent] bf16
             for (int t = 0; t < 4; ++t) {
                 for (int c0 = 0; c0 < HP; c0 += 32) {
                     uint32_t o[32];
@@ -469,13 +486,13 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
             tc::fence_before();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(tc::smem_u32(&sm.o_free));
-            wg_or(false);                           // inv_l is rewritten by the next query
+            wg_or(false);                           // inv_l and the staging tile are reused next query
         }
         if (bad) fail(sm, status);
     }
     tc::fence_before();
     __syncthreads();
-    if (warp == 2) {
+    if (warp == 8) {
         tc::fence_after();
         tc::tmem_dealloc(tmem, TM_COLS);
     }
