@@ -44,6 +44,8 @@ def _args():
     ap.add_argument("--config", type=int, default=3, help="workload index (3 = T=32768 headline)")
     ap.add_argument("--cpu-rows", type=int, default=4096, help="query rows in the CPU-oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only-index", action="store_true",
+                    help="profiling aid: run kpool_build + dsa_index only (no q_lat / out allocation)")
     return ap.parse_args()
 
 
@@ -56,6 +58,19 @@ def _peaks():
                 "bf16_sustained": float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "source": "measured"}
     except (OSError, KeyError, ValueError):
         return {"hbm_gbs": 6800.0, "bf16": 1900.0, "bf16_sustained": 1700.0, "source": "fallback"}
+
+
+# DRAM bytes per query token of the sparse MLA kernel from an ncu capture
+# (dram__bytes_read.sum + dram__bytes_write.sum, T=4096 single document:
+# 538.8 MB / 4096 tokens), keyed by the kernel generation it was taken on.
+MLA_TRAFFIC_PER_TOKEN = {"mla-tc4": 538.8e6 / 4096}
+
+
+def _kernel_tags(K):
+    try:
+        return set(K.version().split()[3:])
+    except Exception:
+        return set()
 
 
 def _work(wl):
@@ -205,6 +220,31 @@ def _config(wl):
             "parallelism": "replicas (one independent forward per GPU)"}
 
 
+def run_index_only(a, wl, inp, K, p, dev):
+    """kpool_build + dsa_index alone on resident inputs (profiling aid)."""
+    import torch
+    d = {"cu_seqlens": torch.from_numpy(inp.cu_seqlens).to(dev), "q_idx": inp.q_idx.to(dev), "k": inp.k.to(dev),
+         "gate": torch.from_numpy(inp.gate).to(dev), "ape": torch.from_numpy(inp.ape).to(dev),
+         "w": torch.from_numpy(inp.w).to(dev)}
+    layout = K.PoolLayout(d["cu_seqlens"], wl.T)
+    kpool = torch.empty((max(wl.T // 4, 1), wl.d_idx), dtype=torch.float32, device=dev)
+    wsb = torch.empty(K.workspace_bytes(p, wl.T, layout.n_docs), dtype=torch.uint8, device=dev)
+    idx = torch.empty((wl.T, wl.W), dtype=torch.int32, device=dev)
+    ev = []
+    for s in range(a.warmup + a.steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        K.kpool_build(d["k"], d["gate"], d["ape"], d["cu_seqlens"], p, kpool_out=kpool, layout=layout)
+        K.dsa_index(d["q_idx"], d["w"], kpool, layout, wl.topk, p, workspace=wsb, indices=idx, W=wl.W)
+        e1.record()
+        if s >= a.warmup:
+            ev.append((e0, e1))
+    torch.cuda.synchronize()
+    ms = statistics.mean(x.elapsed_time(y) for x, y in ev)
+    print(json.dumps({"mode": "index_only", "config": _config(wl), "ms_per_index": ms,
+                      "status": K.check_status(layout.status)}))
+
+
 # ----------------------------------------------------------------- our arm
 
 def main():
@@ -231,12 +271,15 @@ def main():
     K.lib()
 
     wl = workloads.workload(a.config)
-    inp = workloads.all_inputs(wl)
+    inp = workloads.indexer_inputs(wl) if a.only_index else workloads.all_inputs(wl)
     dev = torch.device("cuda", local)
     p = K.make_params(topk=wl.topk, n_idx_heads=wl.n_idx_heads, d_idx=wl.d_idx, n_heads=wl.n_heads,
                       d_lat=wl.d_lat, scale=wl.scale)
     T, W = wl.T, wl.W
 
+    if a.only_index:
+        run_index_only(a, wl, inp, K, p, dev)
+        return
     host = {"cu_seqlens": torch.from_numpy(inp.cu_seqlens), "q_idx": inp.q_idx, "k": inp.k,
             "gate": torch.from_numpy(inp.gate), "ape": torch.from_numpy(inp.ape), "w": torch.from_numpy(inp.w),
             "q_lat": inp.q_lat, "kv_lat": inp.kv_lat}
@@ -336,6 +379,11 @@ def main():
         return
     work = _work(wl)
     peaks = _peaks()
+    tags = _kernel_tags(K)
+    traffic = None
+    for tag, per_tok in MLA_TRAFFIC_PER_TOKEN.items():
+        if tag in tags:
+            traffic = per_tok * wl.T          # scaled from the T=4096 capture (traffic grows with T)
     mla_tflops = work["mla_flops"] / (t["sparse_mla"] / 1e3) / 1e12
     score_tflops = work["score_flops"] / (t["score"] / 1e3) / 1e12
     fp8_peak = 2.0 * peaks["bf16_sustained"]
@@ -349,7 +397,7 @@ def main():
         "stage_ms": t,
         "roofline": {"bound": "tensor", "kernel": "sparse_mla", "achieved": mla_tflops,
                      "peak": peaks["bf16_sustained"], "unit": "TFLOP/s",
-                     "frac": mla_tflops / peaks["bf16_sustained"], "traffic": None,
+                     "frac": mla_tflops / peaks["bf16_sustained"], "traffic": traffic,
                      "peak_kind": f"bf16 sustained, {peaks['source']}",
                      "algorithmic": f"2*H*2D*valid_slots = {work['mla_flops']:.4e} FLOP per launch"},
         "indexer_roofline": {"bound": "tensor", "kernel": "score", "achieved": score_tflops, "peak": fp8_peak,

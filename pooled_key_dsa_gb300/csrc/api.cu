@@ -176,6 +176,8 @@ const char* kpool_strerror(int code) {
     }
 }
 
-const char* kpool_version(void) { return "kpooldsa 0.1 sm_103a"; }
+// The tags after the arch name identify the kernel generations (used to match
+// stored profiler counters to the code that produced them).
+const char* kpool_version(void) { return "kpooldsa 0.2 sm_103a mla-tc4 score-tc1 select1"; }
 
 }  // extern "C"
