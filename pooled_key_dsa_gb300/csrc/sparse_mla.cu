@@ -7,35 +7,46 @@
 // 64 heads.
 //
 // Persistent CTAs (one per SM), each walking query tokens i = blockIdx.x +
-// k*gridDim.x.  For one query the index row is cut into blocks of 32 slots:
-//   S   = Q Kv^T      tcgen05 kind::f16, M = 64 heads, N = 32 slots, K = 512,
-//                     split over two issuing warps (latent 0-255 / 256-511,
-//                     two accumulators the softmax adds)
+// k*gridDim.x.  For one query the index row is cut into blocks of 64 slots:
+//   S   = Q Kv^T      tcgen05 kind::f16, M = 64 heads, N = 64 slots, K = 512,
+//                     split over two issuing warps by latent half; A (Q) is
+//                     read from TMEM, B (the gathered block) from shared memory
 //   O^T += Kv^T P^T   tcgen05 kind::f16, M = 128 latent rows (4 tiles),
-//                     N = 64 heads, K = 32 slots; A is the gathered block read
+//                     N = 64 heads, K = 64 slots; A is the gathered block read
 //                     MN-major, so the tile that fed S also feeds PV
-// Q (64 KB) stays in shared memory for the whole query; gathered latent rows
-// go through a 4-stage ring of 32 KB blocks; S (2 buffers x 2 halves x 32
-// columns) and O^T (4 x 64 columns) live in TMEM.
+// TMEM, 512 columns x 128 lanes:
+//   columns   0-255  O^T, tile t at columns 64t (all lanes)
+//   columns 256-383  Q.  An M=64 operand row r lives in lane 32*(r/16) + r%16
+//                    of subpartition r/16; latent half 0 of every head sits in
+//                    those lanes, latent half 1 in the 16 lanes above them.  An
+//                    M=64 MMA with A in TMEM reads A from the lane half its D is
+//                    written to, so each half of the K sum stays in its half.
+//   columns 384-511  S, two buffers of 64 columns; K half k in lane half k
+// Shared memory holds a 3-stage ring of 64 KB gathered blocks and two P^T tiles.
 //
-// The latent gather from L2 is this kernel's binding resource (about 1 KB per
-// slot, shared by nothing across queries), so four producer warps keep many
+// The latent gather from L2 (about 1 KB per slot, shared by nothing across
+// queries) and the MMA chain of a block bound this kernel.  Four producer warps keep many
 // 16-byte cp.async in flight; each lane's copies arrive on the stage's
 // mbarrier when they land (cp.async.mbarrier.arrive.noinc), so no producer
 // ever waits for a copy, and the MMA issuers take a proxy fence before
-// reading the tile.
+// reading the tile.  The producers also move each query's Q from global memory
+// into TMEM (tcgen05.st) once the previous query's S MMAs are done; they start
+// the gathers of the new query's first blocks before that and prefetch the
+// next query's Q into L2, so a query boundary does not drain the ring.
 //
 // Warp roles (384 threads):
-//   warps 0-3  producers: index scan, Q, latent rows (128-byte swizzle
-//              written by hand), 8 rows of every block per warp
-//   warps 4-7  softmax: the M=64 accumulator sits in lanes 0-15 of each
-//              warp's TMEM subpartition; after the load, lanes 16-31 take the
-//              upper 16 slots of every row, so all 32 lanes work.  The running
-//              max only moves (and O^T is rescaled) when a slot beats it by
-//              more than 2^8; a vote on that is the only barrier of a block in
-//              the common case.  P^T goes to shared memory in the operand
-//              layout; the epilogue writes O^T / l as bf16 through a staging
-//              tile (the P buffers, idle by then).
+//   warps 0-3  producers: index scan, Q rows of TMEM subpartition w, latent
+//              rows (128-byte swizzle written by hand), 16 rows of every
+//              block per warp
+//   warps 4-7  softmax: lane l < 16 loads the K-half-0 row of head 16w+l and
+//              lane l+16 the K-half-1 row; a half-row exchange between the two
+//              leaves lane l with slots 0-31 and lane l+16 with slots 32-63 of
+//              the summed row.  The running max only moves (and O^T is
+//              rescaled) when a slot beats it by more than 2^8; a vote on that
+//              is the only barrier of a block in the common case.  P^T goes to
+//              shared memory in the operand layout; the epilogue writes O^T / l
+//              as bf16 straight from TMEM (lane pairs swap values so that every
+//              store covers two 64-byte runs of output rows).
 //   warps 8-9  S issuers (warp 8 also owns the TMEM allocation)
 //   warp 10    PV issuer
 // Every wait is bounded and warp-uniform (lane 0 polls, the warp takes its
@@ -52,40 +63,40 @@ namespace kpool {
 
 namespace {
 
-constexpr int BN = 32;                 // slots per block
-constexpr int NSTAGE = 4;              // latent-row ring depth
+constexpr int BN = 64;                 // slots per block
+constexpr int NSTAGE = 3;              // latent-row ring depth
 constexpr int NSB = 2;                 // S / P double buffers
 constexpr int HP = 64;                 // head rows (M of S, N of PV)
 constexpr float TAU = 8.0f;            // lazy-rescale threshold (log2 units)
 constexpr int THREADS = 384;
 constexpr int NPROD = 4;               // producer warps
+constexpr int ROWS_PER_PROD = BN / NPROD;
 
-constexpr int Q_BYTES = HP * D_LAT * 2;          // 64 KB: 8 chunks x [64 rows x 128 B]
-constexpr int Q_CHUNK = HP * 128;                // 8 KB
-constexpr int KV_BYTES = BN * D_LAT * 2;         // 32 KB: 8 chunks x [32 rows x 128 B]
-constexpr int KV_CHUNK = BN * 128;               // 4 KB
-constexpr int P_BYTES = HP * 128;                // 8 KB: [64 head rows x 128 B], first 64 B used
+constexpr int KV_BYTES = BN * D_LAT * 2;         // 64 KB: 8 chunks x [64 rows x 128 B]
+constexpr int KV_CHUNK = BN * 128;               // 8 KB
+constexpr int P_BYTES = HP * 128;                // 8 KB: [64 head rows x 128 B] = 64 slots
 
-constexpr int OFF_Q = 0;
-constexpr int OFF_KV = OFF_Q + Q_BYTES;
-constexpr int OFF_P = OFF_KV + NSTAGE * KV_BYTES;        // 2 P buffers = the 16 KB epilogue staging
+constexpr int OFF_KV = 0;
+constexpr int OFF_P = OFF_KV + NSTAGE * KV_BYTES;        // 2 P^T buffers
 constexpr int OFF_SMALL = OFF_P + NSB * P_BYTES;
 
 struct Small {
     uint64_t q_full, q_empty, o_full, o_free, drain;
     uint64_t kv_full[NSTAGE], kv_empty[NSTAGE];
     uint64_t s_full[NSB], s_free[NSB], p_full[NSB], p_empty[NSB], o_step[NSB];
-    uint8_t mask[NSTAGE][NPROD];           // valid-slot bits, 8 slots per producer warp
+    alignas(8) uint16_t mask[NSTAGE][NPROD];   // valid-slot bits, 16 slots per producer warp
     int nb;
     int abort;
     uint32_t tmem;
     float alpha[2][HP];
-    float inv_l[HP];
+    alignas(16) float inv_l[HP];
 };
 constexpr int SMEM_BYTES = OFF_SMALL + (int)sizeof(Small) + 1024;   // + alignment slack
+static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 
 constexpr uint32_t TM_O = 0;           // O^T tile t at columns 64t
-constexpr uint32_t TM_S = 256;         // S buffer b, latent half k at 256 + 64b + 32k
+constexpr uint32_t TM_Q = 256;         // Q, K step kl (16 latent) at 256 + 8kl, lane half = latent half
+constexpr uint32_t TM_S = 384;         // S buffer b at 384 + 64b, lane half = latent half of the sum
 constexpr uint32_t TM_COLS = 512;
 
 constexpr uint32_t ID_S = tc::idesc(64, BN, 1, 1, false, false);
@@ -145,7 +156,7 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
     volatile int* abort_flag = &sm.abort;
 
     if (tid == 0) {
-        tc::mbar_init(tc::smem_u32(&sm.q_full), NPROD * 32 + 1);      // every producer lane's copies + nb
+        tc::mbar_init(tc::smem_u32(&sm.q_full), NPROD);   // each producer warp: its Q rows stored (+ nb)
         tc::mbar_init(tc::smem_u32(&sm.q_empty), 4);      // two S issuers, PV issuer, softmax
         tc::mbar_init(tc::smem_u32(&sm.o_full), 1);
         tc::mbar_init(tc::smem_u32(&sm.o_free), 4);
@@ -172,11 +183,15 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
 
     if (warp < NPROD) {
         // ===================================================== producers
-        // Warp w copies Q rows 16w..16w+15 and rows 8w..8w+7 of every block;
-        // lane l copies 16-byte units l and 32+l of a row.
+        // Warp w: Q rows (heads 16w..16w+15) of TMEM subpartition w, and rows
+        // 16w..16w+15 of every block; lane l copies 16-byte units l and 32+l
+        // of a latent row.
         uint32_t g = 0;                             // global block counter
         uint32_t qn = 0;
         bool ok = true;
+        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        const int qh = warp * 16 + (lane & 15);     // head whose Q row this lane stores
+        const int qhalf = lane >> 4;                // latent half it stores
         for (int i = blockIdx.x; i < T && ok; i += gridDim.x, ++qn) {
             if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
             const int32_t* irow = indices + (int64_t)i * W;
@@ -189,42 +204,61 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
             }
             for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
             const int nb = (last + BN) / BN;
-            // Q tile: the previous query's S MMAs and every reader of nb must be done
-            if (!warp_wait(tc::smem_u32(&sm.q_empty), (qn & 1) ^ 1, abort_flag)) { ok = false; break; }
-            const uint16_t* qsrc = q_lat + (int64_t)i * H * D_LAT;
-#pragma unroll 2
-            for (int rr = 0; rr < HP / NPROD; ++rr) {
-                const int row = warp * (HP / NPROD) + rr;
-                const bool v = row < H;
+            if (warp == 0 && lane == 0 && i + (int)gridDim.x < T)
+                tc::prefetch_l2(q_lat + (int64_t)(i + (int)gridDim.x) * H * D_LAT, (uint32_t)(H * D_LAT * 2));
+
+            // Blocks 0 .. pre-1 need nothing from the previous query and go first;
+            // at b == pre the query's Q is stored (after the previous query's S
+            // MMAs are done).  Lane l < 16 holds the slot index of row 16w + l of
+            // the block, loaded one block ahead.
+            const int pre = nb < NSTAGE - 1 ? nb : NSTAGE - 1;
+            auto slot_of = [&](int b) -> int {
+                const int slot = b * BN + warp * ROWS_PER_PROD + lane;
+                const int v = (lane < ROWS_PER_PROD && slot < W) ? irow[slot] : -1;
+                return (v >= 0 && v < T) ? v : -1;
+            };
+            int nxt = nb > 0 ? slot_of(0) : -1;
+            for (int b = 0; b <= nb; ++b) {
+                if (b == pre) {
+                    // Q: the previous query's S MMAs and every reader of nb must be done
+                    if (!warp_wait(tc::smem_u32(&sm.q_empty), (qn & 1) ^ 1, abort_flag)) { ok = false; break; }
+                    if (nb > 0) {
+                        const bool v = qh < H;
+                        const uint4* qsrc = reinterpret_cast<const uint4*>(
+                            q_lat + ((int64_t)i * H + (v ? qh : 0)) * D_LAT + qhalf * (D_LAT / 2));
+                        // all 32 loads in flight at once, then four 32-column stores
+                        uint32_t r[4][32];
 #pragma unroll
-                for (int k = 0; k < 2; ++k) {
-                    const int u = k * 32 + lane;
-                    tc::cp_async16(s_base + OFF_Q + (u >> 3) * Q_CHUNK + swz(row, u & 7),
-                                   v ? (const void*)(qsrc + row * D_LAT + u * 8) : (const void*)q_lat, v);
+                        for (int c = 0; c < 4; ++c)
+#pragma unroll
+                            for (int j = 0; j < 8; ++j) {
+                                const uint4 x = v ? __ldg(qsrc + c * 8 + j) : make_uint4(0u, 0u, 0u, 0u);
+                                r[c][4 * j] = x.x;
+                                r[c][4 * j + 1] = x.y;
+                                r[c][4 * j + 2] = x.z;
+                                r[c][4 * j + 3] = x.w;
+                            }
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) tc::tmem_st32(tmem + lane_base + TM_Q + 32 * c, r[c]);
+                        tc::tmem_wait_st();
+                    }
+                    tc::fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (warp == 0) sm.nb = nb;
+                        tc::mbar_arrive(tc::smem_u32(&sm.q_full));
+                    }
                 }
-            }
-            tc::cp_async_arrive_noinc(tc::smem_u32(&sm.q_full));
-            if (warp == 0 && lane == 0) {
-                sm.nb = nb;
-                tc::mbar_arrive(tc::smem_u32(&sm.q_full));
-            }
-            for (int b = 0; b < nb; ++b, ++g) {
+                if (b == nb) break;
+                const int myv = nxt;
+                if (b + 1 < nb) nxt = slot_of(b + 1);
                 const int s = g % NSTAGE;
-                if (!warp_wait(tc::smem_u32(&sm.kv_empty[s]), ((g / NSTAGE) & 1) ^ 1, abort_flag)) {
-                    ok = false;
-                    break;
-                }
-                int myv = -1;                       // lane l < 8: slot 8w + l of the block
-                if (lane < 8) {
-                    const int slot = b * BN + warp * 8 + lane;
-                    const int v = slot < W ? irow[slot] : -1;
-                    myv = (v >= 0 && v < T) ? v : -1;
-                }
-                const uint32_t m8 = __ballot_sync(0xffffffffu, myv >= 0) & 0xffu;
+                if (!warp_wait(tc::smem_u32(&sm.kv_empty[s]), ((g / NSTAGE) & 1) ^ 1, abort_flag)) { ok = false; break; }
+                const uint32_t m16 = __ballot_sync(0xffffffffu, myv >= 0) & 0xffffu;
                 const uint32_t dst = s_base + OFF_KV + s * KV_BYTES;
-#pragma unroll
-                for (int rr = 0; rr < 8; ++rr) {
-                    const int row = warp * 8 + rr;
+#pragma unroll 4
+                for (int rr = 0; rr < ROWS_PER_PROD; ++rr) {
+                    const int row = warp * ROWS_PER_PROD + rr;
                     const int v = __shfl_sync(0xffffffffu, myv, rr);
                     const bool valid = v >= 0;
                     const uint16_t* src = valid ? kv_lat + (int64_t)v * D_LAT : kv_lat;
@@ -236,9 +270,10 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
                 }
                 tc::cp_async_arrive_noinc(tc::smem_u32(&sm.kv_full[s]));
                 if (lane == 0) {
-                    sm.mask[s][warp] = (uint8_t)m8;
+                    sm.mask[s][warp] = (uint16_t)m16;
                     tc::mbar_arrive(tc::smem_u32(&sm.kv_full[s]));
                 }
+                ++g;
             }
         }
         tc::cp_async_wait<0>();
@@ -248,17 +283,17 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
         const int half = warp - 8;
         if (lane == 0) {
             uint32_t g = 0, qn = 0;
-            const uint32_t q_addr = s_base + OFF_Q;
+            const uint32_t lh = (uint32_t)(16 * half) << 16;    // lane half of this K half
             bool ok = true;
             for (int i = blockIdx.x; i < T && ok && !*abort_flag; i += gridDim.x, ++qn) {
                 if (!tc::mbar_wait(tc::smem_u32(&sm.q_full), qn & 1, abort_flag)) { ok = false; break; }
-                tc::fence_proxy_async();                // Q was written by cp.async (generic proxy)
+                tc::fence_after();                      // Q was stored with tcgen05.st
                 const int nb = sm.nb;
                 if (nb == 0) {
                     tc::commit(tc::smem_u32(&sm.q_empty));
                     continue;
                 }
-                const uint64_t a0 = tc::sw128_desc(q_addr + half * 4 * Q_CHUNK, 0, 1024);
+                const uint32_t a0 = tmem + lh + TM_Q;
                 for (int b = 0; b < nb; ++b, ++g) {
                     const int s = g % NSTAGE, sb = g % NSB;
                     if (!tc::mbar_wait(tc::smem_u32(&sm.kv_full[s]), (g / NSTAGE) & 1, abort_flag) ||
@@ -269,12 +304,11 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
                     tc::fence_proxy_async();            // the block was written by cp.async
                     tc::fence_after();
                     const uint64_t b0 = tc::sw128_desc(s_base + OFF_KV + s * KV_BYTES + half * 4 * KV_CHUNK, 0, 1024);
-                    const uint32_t d = tmem + TM_S + 64 * sb + 32 * half;
+                    const uint32_t d = tmem + lh + TM_S + 64 * sb;
 #pragma unroll
                     for (int kl = 0; kl < D_LAT / 32; ++kl)      // K steps of 16 latent columns
-                        tc::mma_bf16(d, a0 + (uint64_t)((kl >> 2) * (Q_CHUNK >> 4) + (kl & 3) * 2),
-                                     b0 + (uint64_t)((kl >> 2) * (KV_CHUNK >> 4) + (kl & 3) * 2), ID_S,
-                                     kl > 0 ? 1u : 0u);
+                        tc::mma_bf16_ts(d, a0 + 8u * kl, b0 + (uint64_t)((kl >> 2) * (KV_CHUNK >> 4) + (kl & 3) * 2),
+                                        ID_S, kl > 0 ? 1u : 0u);
                     tc::commit(tc::smem_u32(&sm.s_full[sb]));
                     tc::commit(tc::smem_u32(&sm.kv_empty[s]));
                     if (b == nb - 1) tc::commit(tc::smem_u32(&sm.q_empty));
@@ -331,7 +365,7 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
     } else if (warp >= 4 && warp < 8) {
         // ===================================================== softmax / correction / epilogue
         // Row h = 16*wid + (lane & 15) (head); lane half hs = lane >> 4 owns
-        // slots 16*hs .. 16*hs+15 of the block.  `bad` is sticky per thread and
+        // slots 32*hs .. 32*hs+31 of the block.  `bad` is sticky per thread and
         // ORed across the four warps at every named barrier (bar.red.or).
         const int wid = warp - 4;                   // TMEM subpartition
         const int hs = lane >> 4;
@@ -349,21 +383,21 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
             for (int b = 0; b < nb; ++b, ++g) {
                 const int s = g % NSTAGE, sb = g % NSB;
                 const int cb = g & 1;
-                float x[16];
+                float x[32];
                 bad = bad || !warp_wait(tc::smem_u32(&sm.s_full[sb]), (g / NSB) & 1, abort_flag);
                 if (!bad) {
                     tc::fence_after();
-                    // lanes 0-15 hold whole rows: keep slots 0-15, hand slots 16-31 to lane + 16
+                    // lane l < 16 holds the K-half-0 row, lane l+16 the K-half-1 row of the
+                    // same head; swap halves so that each keeps 32 slots of the sum
                     uint32_t va[32], vb[32];
                     tc::tmem_ld32(tmem + lane_base + TM_S + 64 * sb, va);
                     tc::tmem_ld32(tmem + lane_base + TM_S + 64 * sb + 32, vb);
                     tc::tmem_wait_ld();
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const float lo = __uint_as_float(va[j]) + __uint_as_float(vb[j]);
-                        const float hi = __uint_as_float(va[16 + j]) + __uint_as_float(vb[16 + j]);
-                        const float up = __shfl_sync(0xffffffffu, hi, lane & 15);
-                        x[j] = hs ? up : lo;
+                    for (int j = 0; j < 32; ++j) {
+                        const uint32_t send = hs ? va[j] : vb[j];
+                        const float recv = __uint_as_float(__shfl_xor_sync(0xffffffffu, send, 16));
+                        x[j] = __uint_as_float(hs ? vb[j] : va[j]) + recv;
                     }
                     tc::fence_before();
                     __syncwarp();
@@ -371,11 +405,12 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
                     bad = !warp_wait(tc::smem_u32(&sm.kv_full[s]), (g / NSTAGE) & 1, abort_flag);
                 }
                 const uint32_t mask =
-                    bad ? 0u : ((*reinterpret_cast<volatile uint32_t*>(&sm.mask[s][0]) >> (16 * hs)) & 0xffffu);
+                    bad ? 0u
+                        : (uint32_t)(*reinterpret_cast<volatile uint64_t*>(&sm.mask[s][0]) >> (32 * hs));
                 const float thr = m_ref + TAU;        // -inf for a row that has seen no valid slot yet
                 bool exceed = false;
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
+                for (int j = 0; j < 32; ++j) {
                     x[j] = ((mask >> j) & 1u) ? x[j] * scale_log2 : -INFINITY;
                     exceed |= x[j] > thr;
                 }
@@ -384,7 +419,7 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
                     if (wg_or(bad)) { bad = true; break; }
                     float bmax = -INFINITY;
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) bmax = fmaxf(bmax, x[j]);
+                    for (int j = 0; j < 32; ++j) bmax = fmaxf(bmax, x[j]);
                     bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, 16));
                     float alpha = 1.f;
                     bool need = false;
@@ -419,14 +454,14 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
                         }
                     }
                 }
-                // P^T row h, slots 16*hs .. 16*hs+15: 32 bytes, 16-byte units 2hs, 2hs+1
+                // P^T row h, slots 32*hs .. 32*hs+31: 64 bytes, 16-byte units 4hs .. 4hs+3
                 bad = bad || !warp_wait(tc::smem_u32(&sm.p_empty[sb]), ((g / NSB) & 1) ^ 1, abort_flag);
                 if (!bad) {
-                    uint32_t pk[8];
+                    uint32_t pk[16];
                     float ps = 0.f;
                     const bool live = m_ref != -INFINITY;
 #pragma unroll
-                    for (int j = 0; j < 16; j += 2) {
+                    for (int j = 0; j < 32; j += 2) {
                         const float p0 = live ? fast_exp2(x[j] - m_ref) : 0.f;
                         const float p1 = live ? fast_exp2(x[j + 1] - m_ref) : 0.f;
                         ps += p0 + p1;
@@ -434,8 +469,10 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
                     }
                     l += ps;
                     uint8_t* prow = smem + OFF_P + sb * P_BYTES;
-                    *reinterpret_cast<uint4*>(prow + swz(h, 2 * hs)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-                    *reinterpret_cast<uint4*>(prow + swz(h, 2 * hs + 1)) = make_uint4(pk[4], pk[5], pk[6], pk[7]);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        *reinterpret_cast<uint4*>(prow + swz(h, 4 * hs + k)) =
+                            make_uint4(pk[4 * k], pk[4 * k + 1], pk[4 * k + 2], pk[4 * k + 3]);
                     tc::fence_proxy_async();
                     __syncwarp();
                     if (lane == 0) tc::mbar_arrive(tc::smem_u32(&sm.p_full[sb]));
@@ -452,9 +489,16 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
             }
             if (wg_or(bad)) { bad = true; break; }
             tc::fence_after();
+            // Thread (subpartition wid, lane l) holds latent row 128t + 32wid + l of O^T
+            // tile t for every head.  Lanes l and l^1 swap one value per head pair so
+            // that the even lane writes latent pair (l, l+1) of head 2p and the odd
+            // lane the same pair of head 2p+1: one 4-byte store each, and every store
+            // instruction covers two 64-byte runs of the output rows.
             uint16_t* orow = out + (int64_t)i * H * D_LAT;
-            uint8_t* stg = smem + OFF_P + wid * (HP * 64);        // [64 heads][32 latent] bf16
+            const int odd = lane & 1;
             for (int t = 0; t < 4; ++t) {
+                const int d = t * 128 + wid * 32 + (lane & ~1);
+#pragma unroll 1
                 for (int c0 = 0; c0 < HP; c0 += 32) {
                     uint32_t o[32];
                     if (nb > 0) {
@@ -464,29 +508,30 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
 #pragma unroll
                         for (int j = 0; j < 32; ++j) o[j] = 0u;
                     }
+                    float il[32];
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const float val = __uint_as_float(o[j]) * sm.inv_l[c0 + j];
-                        reinterpret_cast<__nv_bfloat16*>(stg + (c0 + j) * 64)[lane] = __float2bfloat16_rn(val);
+                    for (int j = 0; j < 32; j += 4) {
+                        const float4 q4 = *reinterpret_cast<const float4*>(&sm.inv_l[c0 + j]);
+                        il[j] = q4.x;
+                        il[j + 1] = q4.y;
+                        il[j + 2] = q4.z;
+                        il[j + 3] = q4.w;
+                    }
+#pragma unroll
+                    for (int j = 0; j < 32; j += 2) {
+                        const float a = __uint_as_float(o[j]) * il[j];
+                        const float b = __uint_as_float(o[j + 1]) * il[j + 1];
+                        const float recv = __shfl_xor_sync(0xffffffffu, odd ? a : b, 1);
+                        const uint32_t w = odd ? pack_bf16(recv, b) : pack_bf16(a, recv);
+                        const int hh = c0 + j + odd;
+                        if (hh < H) *reinterpret_cast<uint32_t*>(orow + hh * D_LAT + d) = w;
                     }
                 }
-                __syncwarp();
-                // 64 heads x 64 B: 16-byte stores, 8 per lane
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const int cidx = k * 32 + lane;        // 0..255
-                    const int hh = cidx >> 2, part = cidx & 3;
-                    if (hh < H) {
-                        const uint4 val = *reinterpret_cast<const uint4*>(stg + hh * 64 + part * 16);
-                        *reinterpret_cast<uint4*>(orow + hh * D_LAT + t * 128 + wid * 32 + part * 8) = val;
-                    }
-                }
-                __syncwarp();
             }
             tc::fence_before();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(tc::smem_u32(&sm.o_free));
-            wg_or(false);                           // inv_l and the staging tile are reused next query
+            wg_or(false);                           // inv_l is rewritten next query
         }
         if (bad) fail(sm, status);
     }
