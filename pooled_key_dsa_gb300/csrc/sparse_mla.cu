@@ -35,7 +35,7 @@
 // next query's Q into L2, so a query boundary does not drain the ring.
 //
 // Warp roles (384 threads):
-//   warps 0-3  producers: index scan, Q rows of TMEM subpartition w, latent
+//   warps 0-3  producers: Q rows of TMEM subpartition w, latent
 //              rows (128-byte swizzle written by hand), 16 rows of every
 //              block per warp
 //   warps 4-7  softmax: lane l < 16 loads the K-half-0 row of head 16w+l and
@@ -49,6 +49,8 @@
 //              store covers two 64-byte runs of output rows).
 //   warps 8-9  S issuers (warp 8 also owns the TMEM allocation)
 //   warp 10    PV issuer
+//   warp 11    row scanner: block count and range check of each query's
+//              index row, two queries ahead of the producers
 // Every wait is bounded and warp-uniform (lane 0 polls, the warp takes its
 // answer); on expiry the kernel records KPOOL_ERR_TIMEOUT, the softmax warps
 // agree on stopping at their next named barrier, every role leaves its loop,
@@ -84,7 +86,9 @@ struct Small {
     uint64_t q_full, q_empty, o_full, o_free, drain;
     uint64_t kv_full[NSTAGE], kv_empty[NSTAGE];
     uint64_t s_full[NSB], s_free[NSB], p_full[NSB], p_empty[NSB], o_step[NSB];
+    uint64_t nb_full[2], nb_empty[2];           // row-scan results, two queries deep
     alignas(8) uint16_t mask[NSTAGE][NPROD];   // valid-slot bits, 16 slots per producer warp
+    int nbq[2];                                 // blocks of the scanned query (ring)
     int nb;
     int abort;
     uint32_t tmem;
@@ -161,6 +165,10 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
         tc::mbar_init(tc::smem_u32(&sm.o_full), 1);
         tc::mbar_init(tc::smem_u32(&sm.o_free), 4);
         tc::mbar_init(tc::smem_u32(&sm.drain), 3);
+        for (int r = 0; r < 2; ++r) {
+            tc::mbar_init(tc::smem_u32(&sm.nb_full[r]), 1);        // the row scanner
+            tc::mbar_init(tc::smem_u32(&sm.nb_empty[r]), NPROD);   // every producer warp has read it
+        }
         for (int s = 0; s < NSTAGE; ++s) {
             tc::mbar_init(tc::smem_u32(&sm.kv_full[s]), NPROD * 32 + NPROD);   // copies + masks
             tc::mbar_init(tc::smem_u32(&sm.kv_empty[s]), 3);   // two S issuers + PV issuer
@@ -195,15 +203,11 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
         for (int i = blockIdx.x; i < T && ok; i += gridDim.x, ++qn) {
             if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
             const int32_t* irow = indices + (int64_t)i * W;
-            // last valid slot of the row (entries outside [-1, T) are flagged and skipped)
-            int last = -1;
-            for (int j = lane; j < W; j += 32) {
-                const int v = irow[j];
-                if (v >= 0 && v < T) last = j;
-                else if (v != -1 && warp == 0) set_status(status, KPOOL_ERR_INDEX_RANGE);
-            }
-            for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
-            const int nb = (last + BN) / BN;
+            // the row scanner's block count for this query
+            if (!warp_wait(tc::smem_u32(&sm.nb_full[qn & 1]), (qn >> 1) & 1, abort_flag)) { ok = false; break; }
+            const int nb = sm.nbq[qn & 1];
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(tc::smem_u32(&sm.nb_empty[qn & 1]));
             if (warp == 0 && lane == 0 && i + (int)gridDim.x < T)
                 tc::prefetch_l2(q_lat + (int64_t)(i + (int)gridDim.x) * H * D_LAT, (uint32_t)(H * D_LAT * 2));
 
@@ -362,6 +366,40 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
             }
         }
         __syncwarp();
+    } else if (warp == 11) {
+        // ===================================================== row scanner
+        // For each query of this CTA: the last valid slot of its index row
+        // (entries outside [-1, T) are flagged and skipped) -> block count,
+        // published up to two queries ahead of the producers; rows two queries
+        // ahead are prefetched into L2.
+        uint32_t qn = 0;
+        bool ok = true;
+        for (int i = blockIdx.x; i < T; i += gridDim.x, ++qn) {
+            if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
+            const int r = qn & 1;
+            if (!warp_wait(tc::smem_u32(&sm.nb_empty[r]), ((qn >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
+            const int64_t ahead = (int64_t)i + 2 * (int64_t)gridDim.x;
+            if (lane == 0 && ahead < T && (W & 3) == 0 && ((reinterpret_cast<uintptr_t>(indices) & 15u) == 0))
+                tc::prefetch_l2(indices + ahead * W, (uint32_t)W * 4u);
+            const int32_t* irow = indices + (int64_t)i * W;
+            int last = -1;
+            bool out_of_range = false;
+#pragma unroll 4
+            for (int j = lane; j < W; j += 32) {
+                const int v = __ldg(irow + j);
+                const bool valid = v >= 0 && v < T;
+                last = valid ? j : last;
+                out_of_range |= !valid && v != -1;
+            }
+            for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
+            if (__any_sync(0xffffffffu, out_of_range) && lane == 0) set_status(status, KPOOL_ERR_INDEX_RANGE);
+            if (lane == 0) {
+                sm.nbq[r] = (last + BN) / BN;
+                tc::mbar_arrive(tc::smem_u32(&sm.nb_full[r]));
+            }
+            __syncwarp();
+        }
+        if (!ok) fail(sm, status);
     } else if (warp >= 4 && warp < 8) {
         // ===================================================== softmax / correction / epilogue
         // Row h = 16*wid + (lane & 15) (head); lane half hs = lane >> 4 owns
