@@ -222,28 +222,31 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
                 return (v >= 0 && v < T) ? v : -1;
             };
             int nxt = nb > 0 ? slot_of(0) : -1;
+            // this lane's Q row half (512 B), loaded before the first gathers so that
+            // the load latency hides behind them; stored to TMEM at b == pre
+            uint32_t qr[4][32];
+            {
+                const bool v = nb > 0 && qh < H;
+                const uint4* qsrc = reinterpret_cast<const uint4*>(
+                    q_lat + ((int64_t)i * H + (qh < H ? qh : 0)) * D_LAT + qhalf * (D_LAT / 2));
+#pragma unroll
+                for (int c = 0; c < 4; ++c)
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) {
+                        const uint4 x = v ? __ldg(qsrc + c * 8 + j) : make_uint4(0u, 0u, 0u, 0u);
+                        qr[c][4 * j] = x.x;
+                        qr[c][4 * j + 1] = x.y;
+                        qr[c][4 * j + 2] = x.z;
+                        qr[c][4 * j + 3] = x.w;
+                    }
+            }
             for (int b = 0; b <= nb; ++b) {
                 if (b == pre) {
                     // Q: the previous query's S MMAs and every reader of nb must be done
                     if (!warp_wait(tc::smem_u32(&sm.q_empty), (qn & 1) ^ 1, abort_flag)) { ok = false; break; }
                     if (nb > 0) {
-                        const bool v = qh < H;
-                        const uint4* qsrc = reinterpret_cast<const uint4*>(
-                            q_lat + ((int64_t)i * H + (v ? qh : 0)) * D_LAT + qhalf * (D_LAT / 2));
-                        // all 32 loads in flight at once, then four 32-column stores
-                        uint32_t r[4][32];
 #pragma unroll
-                        for (int c = 0; c < 4; ++c)
-#pragma unroll
-                            for (int j = 0; j < 8; ++j) {
-                                const uint4 x = v ? __ldg(qsrc + c * 8 + j) : make_uint4(0u, 0u, 0u, 0u);
-                                r[c][4 * j] = x.x;
-                                r[c][4 * j + 1] = x.y;
-                                r[c][4 * j + 2] = x.z;
-                                r[c][4 * j + 3] = x.w;
-                            }
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) tc::tmem_st32(tmem + lane_base + TM_Q + 32 * c, r[c]);
+                        for (int c = 0; c < 4; ++c) tc::tmem_st32(tmem + lane_base + TM_Q + 32 * c, qr[c]);
                         tc::tmem_wait_st();
                     }
                     tc::fence_before();
