@@ -168,6 +168,76 @@ int sparse_mla_fwd(const void* q_lat, const void* kv_lat, const int32_t* indices
                    int32_t T, int32_t n_heads, float scale, void* out, float* lse,
                    int32_t* status, kpool_stream_t stream);
 
+/* sparse_mla_fwd_rows: sparse_mla_fwd over a block of n_rows query rows of a
+ * longer sequence.  q_lat, indices, out and lse point at the block's first
+ * row (shapes [n_rows, ...] as for sparse_mla_fwd); kv_lat is the whole
+ * latent [T, 512] and index entries must lie in [-1, T).  Rows are
+ * independent, so the blocks of a split give exactly the unsplit results.
+ * sparse_mla_fwd is this call with n_rows = T. */
+int sparse_mla_fwd_rows(const void* q_lat, const void* kv_lat, const int32_t* indices, int32_t W,
+                        int32_t n_rows, int32_t T, int32_t n_heads, float scale, void* out, float* lse,
+                        int32_t* status, kpool_stream_t stream);
+
+/* kpool_forward_host: the whole forward from host memory, with the copies
+ * overlapped with the kernels.  Host buffers should be page-locked
+ * (cudaHostAlloc / cudaHostRegister); pageable buffers work but their copies
+ * do not overlap.  Shapes are those of kpool_build, dsa_index and
+ * sparse_mla_fwd.  No counterpart on the pages: a pipelined executor of this
+ * library for callers whose inputs and outputs live on the host. */
+typedef struct {
+    const void* k;              /* bf16 [T, d_idx]            */
+    const float* gate;          /* fp32 [T, d_idx]            */
+    const float* ape;           /* fp32 [kpool, d_idx]        */
+    const int32_t* cu_seqlens;  /* int32 [n_docs+1]           */
+    const void* q_idx;          /* bf16 [T, H_i, d_i]         */
+    const float* w;             /* fp32 [T, H_i]              */
+    const void* q_lat;          /* bf16 [T, H, 512]           */
+    const void* kv_lat;         /* bf16 [T, 512]              */
+    void* out;                  /* bf16 [T, H, 512] (written) */
+    float* lse;                 /* fp32 [T, H]      (written) */
+} kpool_host_io;
+
+/* Device buffers of one forward (caller-allocated, alignment as documented
+ * for each call); layout->cu_seqlens must be cu_seqlens below and
+ * layout->T / n_docs must match the call. */
+typedef struct {
+    void* k;
+    float* gate;
+    float* ape;
+    int32_t* cu_seqlens;
+    void* q_idx;
+    float* w;
+    void* q_lat;
+    void* kv_lat;
+    void* out;
+    float* lse;
+    float* kpool;               /* fp32 [max_pools, d_idx]    */
+    kpool_layout* layout;
+    void* workspace;            /* kpool_workspace_bytes(p, T, n_docs) */
+    size_t workspace_bytes;
+    int32_t* indices;           /* int32 [T, W]               */
+    int32_t W;
+} kpool_dev_io;
+
+#define KPOOL_MAX_CHUNKS 64
+
+/* Enqueues, for query rows cut into n_chunks (1..KPOOL_MAX_CHUNKS) blocks:
+ *   s_in:      keys, indexer inputs and kv_lat to the device, then q_lat
+ *              block by block;
+ *   s_compute: kpool_build and dsa_index over all rows (after the inputs
+ *              they read), then sparse_mla_fwd_rows block by block, each
+ *              after its q_lat block has arrived;
+ *   s_out:     out and lse of each block back to the host once its
+ *              attention is done;
+ * and makes s_compute wait for the last copy-out, so the forward is complete
+ * when s_compute is.  The three streams must be distinct, non-default
+ * streams for the copies to overlap.  Device errors go to layout->status;
+ * host-side errors return before or between enqueues (work already
+ * enqueued still runs).  Creates and releases 2*n_chunks+2 CUDA events. */
+int kpool_forward_host(const kpool_host_io* host, const kpool_dev_io* dev, int32_t n_docs, int32_t T,
+                       const kpool_params* p, int32_t n_chunks, kpool_stream_t s_in,
+                       kpool_stream_t s_compute, kpool_stream_t s_out);
+
 /* dsa_index_noalloc: dsa_index for callers that cannot allocate.
  * No counterpart on the pages: this call is an addition of this library.
  * dsa_index needs a caller-allocated workspace; callers that cannot allocate

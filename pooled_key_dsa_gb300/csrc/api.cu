@@ -125,16 +125,110 @@ int dsa_index(const void* q_idx, const float* w, const float* kpool, const kpool
     return stage_mark(3, s);
 }
 
-int sparse_mla_fwd(const void* q_lat, const void* kv_lat, const int32_t* indices, int32_t W, int32_t T,
-                   int32_t n_heads, float scale, void* out, float* lse, int32_t* status, kpool_stream_t stream) {
-    if (T < 0 || W < 1 || n_heads < 1 || n_heads > 64) return KPOOL_ERR_SHAPE;
-    if (T > 0 && (!q_lat || !kv_lat || !indices || !out || !lse)) return KPOOL_ERR_INVALID_ARG;
+int sparse_mla_fwd_rows(const void* q_lat, const void* kv_lat, const int32_t* indices, int32_t W, int32_t n_rows,
+                        int32_t T, int32_t n_heads, float scale, void* out, float* lse, int32_t* status,
+                        kpool_stream_t stream) {
+    if (n_rows < 0 || T < 0 || W < 1 || n_heads < 1 || n_heads > 64) return KPOOL_ERR_SHAPE;
+    if (n_rows > 0 && (!q_lat || !kv_lat || !indices || !out || !lse)) return KPOOL_ERR_INVALID_ARG;
     if (!aligned(q_lat, 16) || !aligned(kv_lat, 16) || !aligned(out, 16) || !aligned(indices, 4))
         return KPOOL_ERR_ALIGN;
     if (!(scale == scale)) return KPOOL_ERR_INVALID_ARG;
-    return launch_sparse_mla(static_cast<const uint16_t*>(q_lat), static_cast<const uint16_t*>(kv_lat), indices, W, T,
-                             n_heads, scale, static_cast<uint16_t*>(out), lse, status,
+    return launch_sparse_mla(static_cast<const uint16_t*>(q_lat), static_cast<const uint16_t*>(kv_lat), indices, W,
+                             n_rows, T, n_heads, scale, static_cast<uint16_t*>(out), lse, status,
                              reinterpret_cast<cudaStream_t>(stream));
+}
+
+int sparse_mla_fwd(const void* q_lat, const void* kv_lat, const int32_t* indices, int32_t W, int32_t T,
+                   int32_t n_heads, float scale, void* out, float* lse, int32_t* status, kpool_stream_t stream) {
+    return sparse_mla_fwd_rows(q_lat, kv_lat, indices, W, T, T, n_heads, scale, out, lse, status, stream);
+}
+
+int kpool_forward_host(const kpool_host_io* h, const kpool_dev_io* d, int32_t n_docs, int32_t T,
+                       const kpool_params* p, int32_t n_chunks, kpool_stream_t s_in, kpool_stream_t s_compute,
+                       kpool_stream_t s_out) {
+    if (!h || !d || !p || !d->layout) return KPOOL_ERR_INVALID_ARG;
+    if (T < 1 || n_docs < 1 || n_chunks < 1 || n_chunks > KPOOL_MAX_CHUNKS) return KPOOL_ERR_SHAPE;
+    if (!h->k || !h->gate || !h->ape || !h->cu_seqlens || !h->q_idx || !h->w || !h->q_lat || !h->kv_lat ||
+        !h->out || !h->lse)
+        return KPOOL_ERR_INVALID_ARG;
+    if (!d->k || !d->gate || !d->ape || !d->cu_seqlens || !d->q_idx || !d->w || !d->q_lat || !d->kv_lat ||
+        !d->out || !d->lse || !d->kpool || !d->workspace || !d->indices)
+        return KPOOL_ERR_INVALID_ARG;
+    if (d->layout->cu_seqlens != d->cu_seqlens || d->layout->T != T || d->layout->n_docs != n_docs)
+        return KPOOL_ERR_INVALID_ARG;
+    if (p->d_lat != D_LAT || p->kpool != KPOOL || p->n_heads < 1 || p->n_heads > 64) return KPOOL_ERR_SHAPE;
+    cudaStream_t si = reinterpret_cast<cudaStream_t>(s_in), sc = reinterpret_cast<cudaStream_t>(s_compute),
+                 so = reinterpret_cast<cudaStream_t>(s_out);
+    const size_t q_row = (size_t)p->n_heads * D_LAT * 2;       // bytes of one q_lat / out row
+    const size_t lse_row = (size_t)p->n_heads * 4;
+    const int32_t rows_per = (T + n_chunks - 1) / n_chunks;
+    n_chunks = (T + rows_per - 1) / rows_per;
+
+    cudaEvent_t ev[2 * KPOOL_MAX_CHUNKS + 2];
+    const int n_ev = 2 * n_chunks + 2;
+    int made = 0, rc = KPOOL_OK;
+    for (; made < n_ev; ++made)
+        if (cudaEventCreateWithFlags(&ev[made], cudaEventDisableTiming) != cudaSuccess) { rc = KPOOL_ERR_CUDA; break; }
+    cudaEvent_t ev_in = ev[0], ev_out = ev[1];
+    cudaEvent_t* ev_q = ev + 2;
+    cudaEvent_t* ev_mla = ev + 2 + n_chunks;
+    auto h2d = [&](void* dst, const void* src, size_t bytes) {
+        if (rc == KPOOL_OK && cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, si) != cudaSuccess)
+            rc = KPOOL_ERR_CUDA;
+    };
+    auto d2h = [&](void* dst, const void* src, size_t bytes) {
+        if (rc == KPOOL_OK && cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToHost, so) != cudaSuccess)
+            rc = KPOOL_ERR_CUDA;
+    };
+    auto ok = [&](cudaError_t e) {
+        if (rc == KPOOL_OK && e != cudaSuccess) rc = KPOOL_ERR_CUDA;
+    };
+    // copy-in stream: keys and indexer inputs, then the query rows chunk by chunk
+    h2d(d->cu_seqlens, h->cu_seqlens, (size_t)(n_docs + 1) * 4);
+    h2d(d->k, h->k, (size_t)T * p->d_idx * 2);
+    h2d(d->gate, h->gate, (size_t)T * p->d_idx * 4);
+    h2d(d->ape, h->ape, (size_t)KPOOL * p->d_idx * 4);
+    h2d(d->kv_lat, h->kv_lat, (size_t)T * D_LAT * 2);
+    h2d(d->q_idx, h->q_idx, (size_t)T * p->n_idx_heads * p->d_idx * 2);
+    h2d(d->w, h->w, (size_t)T * p->n_idx_heads * 4);
+    if (rc == KPOOL_OK) ok(cudaEventRecord(ev_in, si));
+    for (int c = 0; c < n_chunks && rc == KPOOL_OK; ++c) {
+        const int32_t r0 = c * rows_per, n = (T - r0 < rows_per) ? T - r0 : rows_per;
+        h2d(static_cast<uint8_t*>(d->q_lat) + r0 * q_row, static_cast<const uint8_t*>(h->q_lat) + r0 * q_row,
+            (size_t)n * q_row);
+        if (rc == KPOOL_OK) ok(cudaEventRecord(ev_q[c], si));
+    }
+    // compute stream: indexer over all rows, then attention chunk by chunk
+    if (rc == KPOOL_OK) ok(cudaStreamWaitEvent(sc, ev_in, 0));
+    if (rc == KPOOL_OK)
+        rc = kpool_build(d->k, d->gate, d->ape, d->cu_seqlens, n_docs, T, p, d->kpool, d->layout, s_compute);
+    if (rc == KPOOL_OK)
+        rc = dsa_index(d->q_idx, d->w, d->kpool, d->layout, p->topk, p, d->workspace, d->workspace_bytes,
+                       d->indices, d->W, s_compute);
+    for (int c = 0; c < n_chunks && rc == KPOOL_OK; ++c) {
+        const int32_t r0 = c * rows_per, n = (T - r0 < rows_per) ? T - r0 : rows_per;
+        ok(cudaStreamWaitEvent(sc, ev_q[c], 0));
+        if (rc == KPOOL_OK)
+            rc = sparse_mla_fwd_rows(static_cast<const uint8_t*>(d->q_lat) + r0 * q_row, d->kv_lat,
+                                     d->indices + (size_t)r0 * d->W, d->W, n, T, p->n_heads, p->scale,
+                                     static_cast<uint8_t*>(d->out) + r0 * q_row, d->lse + (size_t)r0 * p->n_heads,
+                                     d->layout->status, s_compute);
+        if (rc == KPOOL_OK) ok(cudaEventRecord(ev_mla[c], sc));
+    }
+    // copy-out stream: each chunk's results as soon as its attention is done
+    for (int c = 0; c < n_chunks && rc == KPOOL_OK; ++c) {
+        const int32_t r0 = c * rows_per, n = (T - r0 < rows_per) ? T - r0 : rows_per;
+        ok(cudaStreamWaitEvent(so, ev_mla[c], 0));
+        d2h(static_cast<uint8_t*>(h->out) + r0 * q_row, static_cast<const uint8_t*>(d->out) + r0 * q_row,
+            (size_t)n * q_row);
+        d2h(reinterpret_cast<uint8_t*>(h->lse) + r0 * lse_row,
+            reinterpret_cast<const uint8_t*>(d->lse) + r0 * lse_row, (size_t)n * lse_row);
+    }
+    // the compute stream ends after the last copy-out
+    if (rc == KPOOL_OK) ok(cudaEventRecord(ev_out, so));
+    if (rc == KPOOL_OK) ok(cudaStreamWaitEvent(sc, ev_out, 0));
+    for (int k = 0; k < made; ++k) cudaEventDestroy(ev[k]);   // released once their work completes
+    return rc;
 }
 
 int kpool_stage_select(const float* scores, const int64_t* pair_base, const kpool_layout* layout, int32_t topk,

@@ -48,7 +48,8 @@ int launch_score_mma(const uint8_t* q8, const float* ws, const uint8_t* k8, cons
 int launch_select(const float* scores, const int64_t* pair_base, const kpool_layout& L, int topk, int32_t* indices,
                   int W, cudaStream_t stream);
 
-int launch_sparse_mla(const uint16_t* q_lat, const uint16_t* kv_lat, const int32_t* indices, int W, int T,
-                      int n_heads, float scale, uint16_t* out, float* lse, int32_t* status, cudaStream_t stream);
+int launch_sparse_mla(const uint16_t* q_lat, const uint16_t* kv_lat, const int32_t* indices, int W, int n_rows,
+                      int T, int n_heads, float scale, uint16_t* out, float* lse, int32_t* status,
+                      cudaStream_t stream);
 
 }  // namespace kpool

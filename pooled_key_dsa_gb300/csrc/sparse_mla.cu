@@ -148,8 +148,8 @@ __device__ __forceinline__ bool warp_wait(uint32_t addr, uint32_t parity, const 
 
 __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_t* __restrict__ q_lat,
                                                                   const uint16_t* __restrict__ kv_lat,
-                                                                  const int32_t* __restrict__ indices, int W, int T,
-                                                                  int H, float scale_log2,
+                                                                  const int32_t* __restrict__ indices, int W,
+                                                                  int n_rows, int T, int H, float scale_log2,
                                                                   uint16_t* __restrict__ out,
                                                                   float* __restrict__ lse, int32_t* status) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -200,7 +200,7 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
         const int qh = warp * 16 + (lane & 15);     // head whose Q row this lane stores
         const int qhalf = lane >> 4;                // latent half it stores
-        for (int i = blockIdx.x; i < T && ok; i += gridDim.x, ++qn) {
+        for (int i = blockIdx.x; i < n_rows && ok; i += gridDim.x, ++qn) {
             if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
             const int32_t* irow = indices + (int64_t)i * W;
             // the row scanner's block count for this query
@@ -208,7 +208,7 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
             const int nb = sm.nbq[qn & 1];
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(tc::smem_u32(&sm.nb_empty[qn & 1]));
-            if (warp == 0 && lane == 0 && i + (int)gridDim.x < T)
+            if (warp == 0 && lane == 0 && i + (int)gridDim.x < n_rows)
                 tc::prefetch_l2(q_lat + (int64_t)(i + (int)gridDim.x) * H * D_LAT, (uint32_t)(H * D_LAT * 2));
 
             // Blocks 0 .. pre-1 need nothing from the previous query and go first;
@@ -292,7 +292,7 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
             uint32_t g = 0, qn = 0;
             const uint32_t lh = (uint32_t)(16 * half) << 16;    // lane half of this K half
             bool ok = true;
-            for (int i = blockIdx.x; i < T && ok && !*abort_flag; i += gridDim.x, ++qn) {
+            for (int i = blockIdx.x; i < n_rows && ok && !*abort_flag; i += gridDim.x, ++qn) {
                 if (!tc::mbar_wait(tc::smem_u32(&sm.q_full), qn & 1, abort_flag)) { ok = false; break; }
                 tc::fence_after();                      // Q was stored with tcgen05.st
                 const int nb = sm.nb;
@@ -333,7 +333,7 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
         if (lane == 0) {
             uint32_t g = 0, qn = 0;
             bool ok = true;
-            for (int i = blockIdx.x; i < T && ok && !*abort_flag; i += gridDim.x, ++qn) {
+            for (int i = blockIdx.x; i < n_rows && ok && !*abort_flag; i += gridDim.x, ++qn) {
                 if (!tc::mbar_wait(tc::smem_u32(&sm.q_full), qn & 1, abort_flag)) { ok = false; break; }
                 const int nb = sm.nb;
                 tc::mbar_arrive(tc::smem_u32(&sm.q_empty));   // nb has been read
@@ -377,12 +377,12 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
         // ahead are prefetched into L2.
         uint32_t qn = 0;
         bool ok = true;
-        for (int i = blockIdx.x; i < T; i += gridDim.x, ++qn) {
+        for (int i = blockIdx.x; i < n_rows; i += gridDim.x, ++qn) {
             if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
             const int r = qn & 1;
             if (!warp_wait(tc::smem_u32(&sm.nb_empty[r]), ((qn >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
             const int64_t ahead = (int64_t)i + 2 * (int64_t)gridDim.x;
-            if (lane == 0 && ahead < T && (W & 3) == 0 && ((reinterpret_cast<uintptr_t>(indices) & 15u) == 0))
+            if (lane == 0 && ahead < n_rows && (W & 3) == 0 && ((reinterpret_cast<uintptr_t>(indices) & 15u) == 0))
                 tc::prefetch_l2(indices + ahead * W, (uint32_t)W * 4u);
             const int32_t* irow = indices + (int64_t)i * W;
             int last = -1;
@@ -414,7 +414,7 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
         const uint32_t lane_base = (uint32_t)(wid * 32) << 16;
         uint32_t g = 0, qn = 0;
         bool bad = false;
-        for (int i = blockIdx.x; i < T; i += gridDim.x, ++qn) {
+        for (int i = blockIdx.x; i < n_rows; i += gridDim.x, ++qn) {
             bad = bad || !warp_wait(tc::smem_u32(&sm.q_full), qn & 1, abort_flag);
             if (wg_or(bad)) { bad = true; break; }
             const int nb = sm.nb;
@@ -584,9 +584,10 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
     }
 }
 
-int launch_sparse_mla(const uint16_t* q_lat, const uint16_t* kv_lat, const int32_t* indices, int W, int T,
-                      int n_heads, float scale, uint16_t* out, float* lse, int32_t* status, cudaStream_t stream) {
-    if (T <= 0) return KPOOL_OK;
+int launch_sparse_mla(const uint16_t* q_lat, const uint16_t* kv_lat, const int32_t* indices, int W, int n_rows,
+                      int T, int n_heads, float scale, uint16_t* out, float* lse, int32_t* status,
+                      cudaStream_t stream) {
+    if (n_rows <= 0) return KPOOL_OK;
     if (n_heads < 1 || n_heads > HP) return KPOOL_ERR_SHAPE;
     static int n_sm[64] = {0};
     int dev = 0;
@@ -599,10 +600,10 @@ int launch_sparse_mla(const uint16_t* q_lat, const uint16_t* kv_lat, const int32
         if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return KPOOL_ERR_CUDA;
         n_sm[dev] = sms;
     }
-    const int grid = T < n_sm[dev] ? T : n_sm[dev];
+    const int grid = n_rows < n_sm[dev] ? n_rows : n_sm[dev];
     const float scale_log2 = scale * 1.4426950408889634f;
-    sparse_mla_tc_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(q_lat, kv_lat, indices, W, T, n_heads, scale_log2,
-                                                               out, lse, status);
+    sparse_mla_tc_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(q_lat, kv_lat, indices, W, n_rows, T, n_heads,
+                                                               scale_log2, out, lse, status);
     return cudaGetLastError() == cudaSuccess ? KPOOL_OK : KPOOL_ERR_CUDA;
 }
 

@@ -22,7 +22,7 @@ CODES = {v: k for k, v in ERRORS.items()}
 
 EXPORTED = ("kpool_workspace_bytes", "kpool_workspace_offsets", "kpool_build", "dsa_index", "sparse_mla_fwd",
             "kpool_stage_select", "kpool_set_stage_events", "kpool_check_status", "kpool_strerror", "kpool_version",
-            "dsa_index_noalloc")
+            "dsa_index_noalloc", "sparse_mla_fwd_rows", "kpool_forward_host")
 
 
 class KpoolUnavailable(ImportError):
@@ -47,6 +47,21 @@ class LayoutC(ctypes.Structure):
                 ("pool_tok_start", ctypes.c_void_p), ("tok_doc", ctypes.c_void_p), ("status", ctypes.c_void_p)]
 
 
+class HostIO(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("k", "gate", "ape", "cu_seqlens", "q_idx", "w", "q_lat", "kv_lat",
+                                                "out", "lse")]
+
+
+class DevIO(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in ("k", "gate", "ape", "cu_seqlens", "q_idx", "w", "q_lat", "kv_lat",
+                                                "out", "lse", "kpool")] + \
+               [("layout", ctypes.POINTER(LayoutC)), ("workspace", ctypes.c_void_p),
+                ("workspace_bytes", ctypes.c_size_t), ("indices", ctypes.c_void_p), ("W", ctypes.c_int32)]
+
+
+MAX_CHUNKS = 64
+
+
 class WsOffsets(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in ("q8", "ws", "k8", "s_k", "pair_base", "sched", "scores", "total")]
 
@@ -69,6 +84,9 @@ def lib():
         L.dsa_index.argtypes = [vp, vp, vp, ctypes.POINTER(LayoutC), i32, ctypes.POINTER(Params), vp, sz, vp, i32,
                                 vp]
         L.sparse_mla_fwd.argtypes = [vp, vp, vp, i32, i32, i32, ctypes.c_float, vp, vp, vp, vp]
+        L.sparse_mla_fwd_rows.argtypes = [vp, vp, vp, i32, i32, i32, i32, ctypes.c_float, vp, vp, vp, vp]
+        L.kpool_forward_host.argtypes = [ctypes.POINTER(HostIO), ctypes.POINTER(DevIO), i32, i32,
+                                         ctypes.POINTER(Params), i32, vp, vp, vp]
         L.kpool_stage_select.argtypes = [vp, vp, ctypes.POINTER(LayoutC), i32, vp, i32, vp]
         L.dsa_index_noalloc.argtypes = [vp, vp, vp, ctypes.POINTER(LayoutC), i32, ctypes.POINTER(Params), vp, i32,
                                         vp]
@@ -78,7 +96,8 @@ def lib():
         L.kpool_strerror.restype = ctypes.c_char_p
         L.kpool_version.restype = ctypes.c_char_p
         for name in ("kpool_workspace_offsets", "kpool_build", "dsa_index", "sparse_mla_fwd", "kpool_stage_select",
-                     "kpool_set_stage_events", "kpool_check_status", "dsa_index_noalloc"):
+                     "kpool_set_stage_events", "kpool_check_status", "dsa_index_noalloc", "sparse_mla_fwd_rows",
+                     "kpool_forward_host"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -223,6 +242,59 @@ def sparse_mla_fwd(q_lat, kv_lat, indices, scale: float, out=None, lse=None, sta
     _check(lib().sparse_mla_fwd(_ptr(q_lat), _ptr(kv_lat), _ptr(indices), indices.shape[1], T, H, float(scale),
                                 _ptr(out), _ptr(lse), _ptr(status), _stream(stream)), "sparse_mla_fwd")
     return out, lse
+
+
+def sparse_mla_fwd_rows(q_lat, kv_lat, indices, scale: float, out=None, lse=None, status=None, stream=None):
+    """sparse_mla_fwd over a block of query rows: q_lat [n, H, 512] and indices [n, W] are the block's rows,
+    kv_lat [T, 512] the whole latent (index entries lie in [-1, T))."""
+    n, H, D = q_lat.shape
+    T = kv_lat.shape[0]
+    _want(q_lat, torch.bfloat16, (n, H, D), "q_lat")
+    _want(kv_lat, torch.bfloat16, (T, D), "kv_lat")
+    _want(indices, torch.int32, None, "indices")
+    if indices.dim() != 2 or indices.shape[0] != n:
+        raise ValueError("indices must be [n_rows, W]")
+    if out is None:
+        out = torch.empty_like(q_lat)
+    if lse is None:
+        lse = torch.empty((n, H), dtype=torch.float32, device=q_lat.device)
+    _check(lib().sparse_mla_fwd_rows(_ptr(q_lat), _ptr(kv_lat), _ptr(indices), indices.shape[1], n, T, H,
+                                     float(scale), _ptr(out), _ptr(lse), _ptr(status), _stream(stream)),
+           "sparse_mla_fwd_rows")
+    return out, lse
+
+
+_HOST_KEYS = ("k", "gate", "ape", "cu_seqlens", "q_idx", "w", "q_lat", "kv_lat", "out", "lse")
+
+
+def forward_host(host: dict, dev: dict, layout: PoolLayout, p: Params, n_chunks: int = 8, streams=None):
+    """Whole forward from (page-locked) host tensors with overlapped copies.
+
+    host: CPU tensors k, gate, ape, cu_seqlens, q_idx, w, q_lat, kv_lat (read) and out, lse (written).
+    dev:  CUDA tensors of the same names plus kpool, workspace (uint8) and indices; ``layout`` must be built on
+          dev["cu_seqlens"].  streams: (s_in, s_compute, s_out) torch streams (three new ones by default).
+    Returns s_compute; the forward (including the copies back) is complete when it is."""
+    for name in _HOST_KEYS:
+        t = host[name]
+        if not isinstance(t, torch.Tensor) or t.device.type != "cpu" or not t.is_contiguous():
+            raise TypeError(f"host[{name!r}] must be a contiguous CPU tensor")
+        d = dev[name]
+        _want(d, t.dtype, tuple(t.shape), f"dev[{name!r}]")
+    for name in ("kpool", "workspace", "indices"):
+        if not isinstance(dev[name], torch.Tensor) or dev[name].device.type != "cuda":
+            raise TypeError(f"dev[{name!r}] must be a CUDA tensor")
+    if dev["cu_seqlens"].data_ptr() != layout.c.cu_seqlens:
+        raise ValueError("layout must be built on dev['cu_seqlens']")
+    if streams is None:
+        streams = tuple(torch.cuda.Stream(device=dev["q_lat"].device) for _ in range(3))
+    h = HostIO(*[host[n].data_ptr() for n in _HOST_KEYS])
+    d = DevIO(*[dev[n].data_ptr() for n in _HOST_KEYS], dev["kpool"].data_ptr(), ctypes.pointer(layout.c),
+              dev["workspace"].data_ptr(), dev["workspace"].numel() * dev["workspace"].element_size(),
+              dev["indices"].data_ptr(), dev["indices"].shape[1])
+    _check(lib().kpool_forward_host(ctypes.byref(h), ctypes.byref(d), layout.n_docs, layout.T, ctypes.byref(p),
+                                    int(n_chunks), _stream(streams[0]), _stream(streams[1]), _stream(streams[2])),
+           "kpool_forward_host")
+    return streams[1]
 
 
 def stage_select(scores, pair_base, layout: PoolLayout, topk: int, W=None, indices=None, stream=None):

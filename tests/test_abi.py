@@ -88,6 +88,34 @@ def test_host_checks_reject_bad_arguments(lib):
     assert lib.kpool_check_status(None, None) == K.CODES["KPOOL_ERR_INVALID_ARG"]
 
 
+def test_host_checks_of_the_row_block_and_host_pipeline_entries(lib):
+    vp = ctypes.c_void_p
+    # row blocks: negative row count, misaligned q_lat, zero rows is a no-op
+    assert lib.sparse_mla_fwd_rows(vp(16), vp(16), vp(16), 128, -1, 64, 64, 0.1, vp(16), vp(16), None,
+                                   None) == K.CODES["KPOOL_ERR_SHAPE"]
+    assert lib.sparse_mla_fwd_rows(vp(8), vp(16), vp(16), 128, 4, 64, 64, 0.1, vp(16), vp(16), None,
+                                   None) == K.CODES["KPOOL_ERR_ALIGN"]
+    assert lib.sparse_mla_fwd_rows(None, None, None, 128, 0, 64, 64, 0.1, None, None, None, None) == K.KPOOL_OK
+    # host pipeline: fake non-null pointers; chunk counts, nulls and layout mismatches are refused before any
+    # CUDA call
+    p = K.make_params()
+    lay = K.LayoutC(1, 64, 16, 16, 16, 16, 16, 16)
+    h = K.HostIO(*([16] * 10))
+    d = K.DevIO(*([16] * 11), ctypes.pointer(lay), 16, 1 << 30, 16, 2176)
+    for n_chunks in (0, K.MAX_CHUNKS + 1):
+        assert lib.kpool_forward_host(ctypes.byref(h), ctypes.byref(d), 1, 64, ctypes.byref(p), n_chunks, None, None,
+                                      None) == K.CODES["KPOOL_ERR_SHAPE"]
+    h_null = K.HostIO(*([16] * 9 + [0]))
+    assert lib.kpool_forward_host(ctypes.byref(h_null), ctypes.byref(d), 1, 64, ctypes.byref(p), 4, None, None,
+                                  None) == K.CODES["KPOOL_ERR_INVALID_ARG"]
+    lay_other = K.LayoutC(1, 64, 16, 32, 16, 16, 16, 16)     # built on another cu_seqlens
+    d_other = K.DevIO(*([16] * 11), ctypes.pointer(lay_other), 16, 1 << 30, 16, 2176)
+    assert lib.kpool_forward_host(ctypes.byref(h), ctypes.byref(d_other), 1, 64, ctypes.byref(p), 4, None, None,
+                                  None) == K.CODES["KPOOL_ERR_INVALID_ARG"]
+    assert lib.kpool_forward_host(ctypes.byref(h), ctypes.byref(d), 1, 32, ctypes.byref(p), 4, None, None,
+                                  None) == K.CODES["KPOOL_ERR_INVALID_ARG"]     # layout T differs
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(K, "_lib", None)
     monkeypatch.setattr(K, "_LIB_PATH", str(tmp_path / "missing.so"))
