@@ -63,8 +63,9 @@ def _peaks():
 
 # DRAM bytes per query token of the sparse MLA kernel from an ncu capture
 # (dram__bytes_read.sum + dram__bytes_write.sum, T=4096 single document:
-# 538.8 MB / 4096 tokens), keyed by the kernel generation it was taken on.
-MLA_TRAFFIC_PER_TOKEN = {"mla-tc4": 538.8e6 / 4096}
+# 308.6 + 228.6 MB / 4096 tokens), keyed by the kernel generation it was
+# taken on; another generation reports null until it is captured.
+MLA_TRAFFIC_PER_TOKEN = {"mla-tc5": 537.2e6 / 4096}
 
 
 def _kernel_tags(K):

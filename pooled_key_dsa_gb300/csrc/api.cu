@@ -272,6 +272,6 @@ const char* kpool_strerror(int code) {
 
 // The tags after the arch name identify the kernel generations (used to match
 // stored profiler counters to the code that produced them).
-const char* kpool_version(void) { return "kpooldsa 0.2 sm_103a mla-tc4 score-tc1 select1"; }
+const char* kpool_version(void) { return "kpooldsa 0.3 sm_103a mla-tc5 score-tc1 select2"; }
 
 }  // extern "C"

@@ -6,7 +6,15 @@
 // PR "add GLM-5.3-Flash training support": 2048 + 3 = 2051 raw slots.
 //
 // One 256-thread block per query row.  Scores become order-preserving uint32
-// keys; a three-level radix select (bits 31..20, 19..8, 7..0) finds the key K
+// keys.  Rows of up to 8192 candidate pools (every row of a document of up to
+// 32768 tokens) take the register path: each thread holds 32 keys (pools
+// t, t+256, ...; loads coalesced), a three-level radix select (bits 31..21,
+// 20..10, 9..0) over the registers finds the key K of the topk-th best pool
+// and how many pools equal to K still fit, and the ordered compaction ranks
+// the kept pools with one ballot per 256-pool column and one block scan over
+// the (column, warp) counts.  Longer rows take the streaming path below.
+//
+// Streaming path: a three-level radix select (bits 31..20, 19..8, 7..0) finds the key K
 // of the topk-th best pool and how many pools equal to K still fit
 // (`need_eq`).  Level 1 histograms every key; the pools in the chosen level-1
 // bin are copied to a shared candidate list that levels 2 and 3 refine (if the
@@ -88,9 +96,99 @@ __device__ void pick_digit(SelectSmem& s, int nbins, uint32_t remaining) {
     __syncthreads();
 }
 
+constexpr int FAST_KPT = 32;                          // keys per thread on the register path
+constexpr int FAST_MAX = SEL_THREADS * FAST_KPT;     // 8192 candidate pools
+
+// One radix level over register-held keys: histogram of bits [shift, shift+log2(nbins)) of the
+// valid keys whose bits above match `prefix` under `hi_mask`, then the digit that holds the
+// remaining-th largest key (s.digit, s.remaining).
+template <int NC>
+__device__ __forceinline__ void fast_level(SelectSmem& s, const uint32_t (&key)[NC], uint32_t valid,
+                                           uint32_t hi_mask, uint32_t prefix, int shift, int nbins,
+                                           uint32_t remaining) {
+    for (int b = threadIdx.x; b < nbins; b += SEL_THREADS) s.hist[b] = 0;
+    __syncthreads();
+#pragma unroll
+    for (int j = 0; j < NC; ++j)
+        if (((valid >> j) & 1u) && (key[j] & hi_mask) == prefix)
+            atomicAdd(&s.hist[(key[j] >> shift) & (uint32_t)(nbins - 1)], 1u);
+    __syncthreads();
+    pick_digit(s, nbins, remaining);
+}
+
+// Ranks, in pool order, of per-thread flags held as one bit per column: afterwards pool
+// 256j + t has rank tab[8j + warp] + popc(bal[j] & lanes below).  tab (256 entries, one per
+// (column, warp) in that order) holds the exclusive scan of the per-(column, warp) counts.
+// The caller reads tab, then synchronises before tab is reused.
+template <int NC>
+__device__ __forceinline__ void column_scan(SelectSmem& s, uint32_t flags, uint32_t (&bal)[NC]) {
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    uint32_t* tab = s.cand_key;                      // free on this path
+#pragma unroll
+    for (int j = 0; j < NC; ++j) {
+        bal[j] = __ballot_sync(0xffffffffu, (flags >> j) & 1u);
+        if (lane == 0) tab[8 * j + wid] = __popc(bal[j]);
+    }
+    __syncthreads();
+    int total;
+    const int before = block_excl_scan(threadIdx.x < 8 * NC ? (int)tab[threadIdx.x] : 0, s.warp_tot, total);
+    tab[threadIdx.x] = (uint32_t)before;
+    __syncthreads();
+}
+
+template <int NC>
+__device__ void select_registers(SelectSmem& s, const float* __restrict__ sc, int n, int topk, int s_d,
+                                 int32_t* __restrict__ row) {
+    const int t = threadIdx.x, wid = t >> 5;
+    const uint32_t below = (1u << (t & 31)) - 1u;
+    const uint32_t* tab = s.cand_key;
+    uint32_t key[NC];
+    uint32_t valid = 0;
+#pragma unroll
+    for (int j = 0; j < NC; ++j) {
+        const int p = SEL_THREADS * j + t;
+        key[j] = p < n ? score_key(sc[p]) : 0u;
+        valid |= (p < n ? 1u : 0u) << j;
+    }
+    fast_level(s, key, valid, 0u, 0u, 21, 2048, (uint32_t)topk);
+    uint32_t prefix = s.digit << 21;
+    fast_level(s, key, valid, 0xFFE00000u, prefix, 10, 2048, s.remaining);
+    prefix |= s.digit << 10;
+    fast_level(s, key, valid, 0xFFFFFC00u, prefix, 0, 1024, s.remaining);
+    const uint32_t K = prefix | s.digit;
+    const uint32_t need_eq = s.remaining;
+    const uint32_t n_eq = s.hist[s.digit & 1023u];   // keys equal to K
+    __syncthreads();
+
+    uint32_t gt = 0, eq = 0;
+#pragma unroll
+    for (int j = 0; j < NC; ++j) {
+        gt |= (((valid >> j) & 1u) && key[j] > K ? 1u : 0u) << j;
+        eq |= (((valid >> j) & 1u) && key[j] == K ? 1u : 0u) << j;
+    }
+    uint32_t take = gt | eq;
+    uint32_t bal[NC];
+    if (n_eq != need_eq) {                           // ties at K: the lowest pool indices among them win
+        column_scan(s, eq, bal);
+#pragma unroll
+        for (int j = 0; j < NC; ++j)
+            if (((eq >> j) & 1u) && tab[8 * j + wid] + __popc(bal[j] & below) >= need_eq) take &= ~(1u << j);
+        __syncthreads();
+    }
+    column_scan(s, take, bal);
+#pragma unroll
+    for (int j = 0; j < NC; ++j) {
+        const uint32_t rank = tab[8 * j + wid] + __popc(bal[j] & below);
+        if (((take >> j) & 1u) && rank < (uint32_t)topk) {
+            const int pos = s_d + KPOOL * (SEL_THREADS * j + t);
+            *reinterpret_cast<int4*>(row + KPOOL * rank) = make_int4(pos, pos + 1, pos + 2, pos + 3);
+        }
+    }
+}
+
 }  // namespace
 
-__global__ void __launch_bounds__(SEL_THREADS) select_kernel(const float* __restrict__ scores,
+__global__ void __launch_bounds__(SEL_THREADS, 3) select_kernel(const float* __restrict__ scores,
                                                              const int64_t* __restrict__ pair_base,
                                                              const int32_t* __restrict__ cu_seqlens,
                                                              const int32_t* __restrict__ cu_pools,
@@ -114,6 +212,16 @@ __global__ void __launch_bounds__(SEL_THREADS) select_kernel(const float* __rest
         return;
     }
     const float* sc = scores + pair_base[d] + pairs_before(r);
+    if (n <= FAST_MAX) {
+        if (n <= 8 * SEL_THREADS) select_registers<8>(s, sc, n, topk, s_d, row);
+        else if (n <= 16 * SEL_THREADS) select_registers<16>(s, sc, n, topk, s_d, row);
+        else select_registers<32>(s, sc, n, topk, s_d, row);
+        for (int j = KPOOL * topk + t; j < W; j += SEL_THREADS) {
+            const int q = j - KPOOL * topk;
+            row[j] = q < tail ? i - tail + 1 + q : -1;
+        }
+        return;
+    }
 
     // ---- level 1: bits 31..20 over all keys
     for (int b = t; b < HIST_BINS; b += SEL_THREADS) s.hist[b] = 0;
