@@ -262,7 +262,8 @@ int dsa_index_noalloc(const void* q_idx, const float* w, const float* kpool, con
 /* Stage entry point: top-k select + row expansion alone, fed with scores in
  * the workspace's compact layout (same rules as dsa_index's last step).
  *   scores   fp32, compact triangle as described for kpool_ws_offsets
- *   pair_base int64 [n_docs+1] as described there */
+ *            (16-byte aligned, as the workspace's scores are)
+ *   pair_base int64 [n_docs+1] as described there (8-byte aligned) */
 int kpool_stage_select(const float* scores, const int64_t* pair_base, const kpool_layout* layout,
                        int32_t topk, int32_t* indices, int32_t W, kpool_stream_t stream);
 

@@ -236,7 +236,7 @@ int kpool_stage_select(const float* scores, const int64_t* pair_base, const kpoo
     if (!layout_ok(layout) || topk < 1 || !pair_base || (layout->T > 0 && (!scores || !indices)))
         return KPOOL_ERR_INVALID_ARG;
     if ((int64_t)W < (int64_t)KPOOL * topk + KPOOL - 1 || W % 4 != 0) return KPOOL_ERR_SHAPE;
-    if (!aligned(indices, 16) || !aligned(pair_base, 8)) return KPOOL_ERR_ALIGN;
+    if (!aligned(indices, 16) || !aligned(pair_base, 8) || !aligned(scores, 16)) return KPOOL_ERR_ALIGN;
     return launch_select(scores, pair_base, *layout, topk, indices, W, reinterpret_cast<cudaStream_t>(stream));
 }
 

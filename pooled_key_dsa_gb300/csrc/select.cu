@@ -188,41 +188,11 @@ __device__ void select_registers(SelectSmem& s, const float* __restrict__ sc, in
 
 }  // namespace
 
-__global__ void __launch_bounds__(SEL_THREADS, 3) select_kernel(const float* __restrict__ scores,
-                                                             const int64_t* __restrict__ pair_base,
-                                                             const int32_t* __restrict__ cu_seqlens,
-                                                             const int32_t* __restrict__ cu_pools,
-                                                             const int32_t* __restrict__ tok_doc, int n_docs, int T,
-                                                             int topk, int32_t* __restrict__ indices, int W) {
-    __shared__ SelectSmem s;
-    const int i = blockIdx.x;
+// Streaming path for rows of more than FAST_MAX candidate pools: the row is
+// read from global memory on every pass.
+__device__ void select_streaming(SelectSmem& s, const float* __restrict__ sc, int n, int topk, int s_d, int i,
+                                 int tail, int32_t* __restrict__ row, int W) {
     const int t = threadIdx.x;
-    int32_t* row = indices + (int64_t)i * W;
-    const int d = (cu_pools[n_docs] < 0) ? -1 : tok_doc[i];
-    if (d < 0) {
-        for (int j = t; j < W; j += SEL_THREADS) row[j] = -1;
-        return;
-    }
-    const int s_d = cu_seqlens[d];
-    const int r = i - s_d;
-    const int n = (r + 1) / KPOOL;
-    const int tail = (r + 1) % KPOOL;
-    if (n <= topk) {                                  // every candidate is kept: the causal prefix
-        for (int j = t; j < W; j += SEL_THREADS) row[j] = (j <= r) ? s_d + j : -1;
-        return;
-    }
-    const float* sc = scores + pair_base[d] + pairs_before(r);
-    if (n <= FAST_MAX) {
-        if (n <= 8 * SEL_THREADS) select_registers<8>(s, sc, n, topk, s_d, row);
-        else if (n <= 16 * SEL_THREADS) select_registers<16>(s, sc, n, topk, s_d, row);
-        else select_registers<32>(s, sc, n, topk, s_d, row);
-        for (int j = KPOOL * topk + t; j < W; j += SEL_THREADS) {
-            const int q = j - KPOOL * topk;
-            row[j] = q < tail ? i - tail + 1 + q : -1;
-        }
-        return;
-    }
-
     // ---- level 1: bits 31..20 over all keys
     for (int b = t; b < HIST_BINS; b += SEL_THREADS) s.hist[b] = 0;
     if (t == 0) s.n_cand = 0;
@@ -303,11 +273,125 @@ __global__ void __launch_bounds__(SEL_THREADS, 3) select_kernel(const float* __r
     }
 }
 
+
+// Row metadata: document, in-document position, candidate count and the
+// element offset of the row's scores in the compact triangle.
+struct RowInfo {
+    int d, s_d, r, n, tail;
+    int64_t start;
+};
+
+__device__ __forceinline__ RowInfo row_info(int i, const int64_t* __restrict__ pair_base,
+                                            const int32_t* __restrict__ cu_seqlens,
+                                            const int32_t* __restrict__ cu_pools, const int32_t* __restrict__ tok_doc,
+                                            int n_docs) {
+    RowInfo ri;
+    ri.d = (cu_pools[n_docs] < 0) ? -1 : tok_doc[i];
+    ri.s_d = ri.r = ri.n = ri.tail = 0;
+    ri.start = 0;
+    if (ri.d >= 0) {
+        ri.s_d = cu_seqlens[ri.d];
+        ri.r = i - ri.s_d;
+        ri.n = (ri.r + 1) / KPOOL;
+        ri.tail = (ri.r + 1) % KPOOL;
+        ri.start = pair_base[ri.d] + pairs_before(ri.r);
+    }
+    return ri;
+}
+
+constexpr int ROWBUF = FAST_MAX + 8;                  // floats per row buffer (+ alignment slack)
+
+// Asynchronous copy of a row's n scores into `buf` (16-byte units from the unit
+// holding the first score; the last unit copies only the bytes of the row).
+// The first score is buf[start % 4].
+__device__ __forceinline__ void prefetch_row(float* buf, const float* __restrict__ scores, int64_t start, int n) {
+    const int64_t b0 = start * 4, b1 = (start + n) * 4;
+    const int64_t u0 = b0 >> 4, u1 = (b1 + 15) >> 4;
+    const char* base = reinterpret_cast<const char*>(scores);
+    const uint32_t dst0 = static_cast<uint32_t>(__cvta_generic_to_shared(buf));
+    for (int64_t u = u0 + threadIdx.x; u < u1; u += SEL_THREADS) {
+        const int64_t off = u * 16;
+        const int64_t rem = b1 - off;
+        const uint32_t bytes = rem < 16 ? (uint32_t)rem : 16u;
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst0 + (uint32_t)(u - u0) * 16u),
+                     "l"(base + off), "r"(bytes)
+                     : "memory");
+    }
+}
+
+__device__ __forceinline__ bool fast_row(const RowInfo& ri, int topk) {
+    return ri.d >= 0 && ri.n > topk && ri.n <= FAST_MAX;
+}
+
+// Persistent: block b walks rows b, b + gridDim.x, ...; the scores of the
+// next row are copied into shared memory (cp.async) while the current row is
+// ranked, so the load latency of a row is hidden behind the previous one.
+__global__ void __launch_bounds__(SEL_THREADS, 2) select_kernel(const float* __restrict__ scores,
+                                                             const int64_t* __restrict__ pair_base,
+                                                             const int32_t* __restrict__ cu_seqlens,
+                                                             const int32_t* __restrict__ cu_pools,
+                                                             const int32_t* __restrict__ tok_doc, int n_docs, int T,
+                                                             int topk, int32_t* __restrict__ indices, int W) {
+    __shared__ SelectSmem s;
+    extern __shared__ __align__(16) float rowbuf[];   // 2 x ROWBUF
+    const int t = threadIdx.x;
+    int i = blockIdx.x;
+    if (i >= T) return;
+    RowInfo cur = row_info(i, pair_base, cu_seqlens, cu_pools, tok_doc, n_docs);
+    if (fast_row(cur, topk)) prefetch_row(rowbuf, scores, cur.start, cur.n);
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
+    for (int k = 0; i < T; ++k, i += gridDim.x) {
+        const int i2 = i + (int)gridDim.x;
+        RowInfo nxt;
+        nxt.d = -1;
+        if (i2 < T) {
+            nxt = row_info(i2, pair_base, cu_seqlens, cu_pools, tok_doc, n_docs);
+            if (fast_row(nxt, topk)) prefetch_row(rowbuf + ((k + 1) & 1) * ROWBUF, scores, nxt.start, nxt.n);
+        }
+        asm volatile("cp.async.commit_group;\n" ::: "memory");
+
+        int32_t* row = indices + (int64_t)i * W;
+        if (cur.d < 0) {
+            for (int j = t; j < W; j += SEL_THREADS) row[j] = -1;
+        } else if (cur.n <= topk) {                   // every candidate is kept: the causal prefix
+            for (int j = t; j < W; j += SEL_THREADS) row[j] = (j <= cur.r) ? cur.s_d + j : -1;
+        } else if (cur.n <= FAST_MAX) {
+            asm volatile("cp.async.wait_group 1;\n" ::: "memory");
+            __syncthreads();
+            const float* sc = rowbuf + (k & 1) * ROWBUF + (int)(cur.start & 3);
+            if (cur.n <= 8 * SEL_THREADS) select_registers<8>(s, sc, cur.n, topk, cur.s_d, row);
+            else if (cur.n <= 16 * SEL_THREADS) select_registers<16>(s, sc, cur.n, topk, cur.s_d, row);
+            else select_registers<32>(s, sc, cur.n, topk, cur.s_d, row);
+            for (int j = KPOOL * topk + t; j < W; j += SEL_THREADS) {
+                const int q = j - KPOOL * topk;
+                row[j] = q < cur.tail ? i - cur.tail + 1 + q : -1;
+            }
+        } else {
+            select_streaming(s, scores + cur.start, cur.n, topk, cur.s_d, i, cur.tail, row, W);
+        }
+        __syncthreads();                              // the row buffer and s are reused
+        cur = nxt;
+    }
+    asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+}
+
 int launch_select(const float* scores, const int64_t* pair_base, const kpool_layout& L, int topk, int32_t* indices,
                   int W, cudaStream_t stream) {
     if (L.T <= 0) return KPOOL_OK;
-    select_kernel<<<L.T, SEL_THREADS, 0, stream>>>(scores, pair_base, L.cu_seqlens, L.cu_pools, L.tok_doc, L.n_docs,
-                                                  L.T, topk, indices, W);
+    constexpr int kDyn = 2 * ROWBUF * (int)sizeof(float);
+    static int n_sm[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return KPOOL_ERR_CUDA;
+    if (n_sm[dev] == 0) {
+        if (cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDyn) != cudaSuccess)
+            return KPOOL_ERR_CUDA;
+        int sms = 0;
+        if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return KPOOL_ERR_CUDA;
+        n_sm[dev] = sms;
+    }
+    const int grid = L.T < 2 * n_sm[dev] ? L.T : 2 * n_sm[dev];
+    select_kernel<<<grid, SEL_THREADS, kDyn, stream>>>(scores, pair_base, L.cu_seqlens, L.cu_pools, L.tok_doc,
+                                                      L.n_docs, L.T, topk, indices, W);
     return cudaGetLastError() == cudaSuccess ? KPOOL_OK : KPOOL_ERR_CUDA;
 }
 
