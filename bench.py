@@ -371,6 +371,24 @@ def main():
         if s >= 0:
             e2e_ev[s][1].record(streams[1])
     torch.cuda.synchronize()
+    # ---- IndexShare: a shared DSA layer (its own q_lat / kv_lat) on the index rows just computed;
+    # it runs the sparse attention only
+    q1_h, kv1_h = workloads.layer_attention_inputs(wl, 1)
+    q1, kv1 = q1_h.to(dev), kv1_h.to(dev)
+    del q1_h, kv1_h
+    out1 = torch.empty_like(q1)
+    lse1 = torch.empty_like(lse)
+    is_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(a.steps)]
+    for s in range(-1, a.steps):
+        flush.zero_()
+        if s >= 0:
+            is_ev[s][0].record(stream)
+        K.sparse_mla_fwd(q1, kv1, idx, wl.scale, out=out1, lse=lse1, status=layout.status)
+        if s >= 0:
+            is_ev[s][1].record(stream)
+    torch.cuda.synchronize()
+    is_ms = statistics.mean(x.elapsed_time(y) for x, y in is_ev)
+    del q1, kv1, out1, lse1
     e2e_ms = sum(x.elapsed_time(y) for x, y in e2e_ev)
     tm = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
     if world > 1:
@@ -412,6 +430,8 @@ def main():
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "api": f"kpool_forward_host, {a.chunks} query-row blocks, page-locked host buffers"},
         "gpu_launches": LAUNCHES_PER_STEP * a.steps,
+        "indexshare_layer": {"ms": is_ms, "tokens_per_s": T / (is_ms / 1e3),
+                             "what": "a shared DSA layer: sparse_mla_fwd only, on the index rows of the step"},
         "wall_s_timed": wall,
     }
     if world == 1 and not a.no_cpu_baseline:

@@ -179,6 +179,20 @@ def q_lat(wl: Workload, rows=None) -> torch.Tensor:
     return _chunked_bf16(wl.seed, _QLAT, wl.T, (wl.n_heads, wl.d_lat), rows=rows)
 
 
+# tensor ids of a further layer's attention inputs: _QLAT + _LAYER_STRIDE * layer, ...
+_LAYER_STRIDE = 16
+
+
+def layer_attention_inputs(wl: Workload, layer: int, rows=None) -> tuple:
+    """(q_lat [T, H, D] or the given rows of it, kv_lat [T, D]) of DSA layer ``layer`` of a stack whose
+    layers share this workload's index rows (IndexShare: the indexer runs in layer 0 only).  Layer 0 gives
+    the workload's own attention inputs; each further layer has its own seeded streams."""
+    off = _LAYER_STRIDE * int(layer)
+    q = _chunked_bf16(wl.seed, _QLAT + off, wl.T, (wl.n_heads, wl.d_lat), rows=rows)
+    kv = _chunked_bf16(wl.seed, _KVLAT + off, wl.T, (wl.d_lat,))
+    return q, kv
+
+
 def all_inputs(wl: Workload) -> Inputs:
     inp = indexer_inputs(wl)
     inp.q_lat = q_lat(wl)
