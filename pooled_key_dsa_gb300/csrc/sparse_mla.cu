@@ -360,7 +360,13 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
                     tc::commit(tc::smem_u32(&sm.o_step[sb]));
                 }
                 if (!ok) break;
-                tc::commit(tc::smem_u32(&sm.o_full));      // once per query, also for an empty row
+                // once per query, also for an empty row; an empty row still waits for the
+                // previous epilogue so that o_full and o_free strictly alternate
+                if (nb == 0 && !tc::mbar_wait(tc::smem_u32(&sm.o_free), (qn & 1) ^ 1, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc::commit(tc::smem_u32(&sm.o_full));
             }
             if (!ok) fail(sm, status);
             tc::commit(tc::smem_u32(&sm.drain));

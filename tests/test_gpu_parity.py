@@ -309,3 +309,31 @@ def test_determinism_and_document_isolation():
     kv2[s:] = 1.0
     o2, l2 = K.sparse_mla_fwd(ql, kv2, c["indices_dev"], wl.scale)
     assert torch.equal(o1[:s], o2[:s]) and torch.equal(l1[:s], l2[:s])
+
+
+def test_sparse_mla_runs_of_empty_rows():
+    # Each CTA walks rows i, i + n_sm, ...; whole bands of empty rows give every CTA
+    # consecutive empty queries, between and after non-empty ones.
+    wl = workloads.custom("mla_empty_runs", 11, (1900,), n_heads=64)
+    inp = workloads.indexer_inputs(wl)
+    ql = workloads.q_lat(wl)
+    T, W = wl.T, 256
+    n_sm = torch.cuda.get_device_properties(0).multi_processor_count
+    rng = np.random.default_rng(1)
+    idx = np.full((T, W), -1, np.int32)
+    for i in range(T):
+        band = (i // n_sm) % 4
+        if band in (1, 2):
+            continue                              # two consecutive empty queries per CTA
+        n = int(rng.integers(1, W + 1))
+        idx[i, :n] = np.sort(rng.choice(T, n, replace=False))
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, lse = K.sparse_mla_fwd(ql.cuda(), inp.kv_lat.cuda(), torch.from_numpy(idx).cuda(), wl.scale, status=st)
+    assert K.check_status(st) == 0
+    rows = np.arange(T)
+    out_o, lse_o = O.sparse_attention(ql.float().numpy(), inp.kv_lat.float().numpy(), idx, wl.scale, rows)
+    out_g, lse_g = out.float().cpu().numpy(), lse.cpu().numpy()
+    empty = np.all(idx < 0, axis=1)
+    assert np.all(out_g[empty] == 0) and np.all(np.isneginf(lse_g[empty]))
+    mx, mean, le = KP.attention_check(out_g[~empty], lse_g[~empty], out_o[~empty], lse_o[~empty])
+    assert mx <= KP.OUT_MAX_ABS and mean <= KP.OUT_MEAN_ABS and le <= KP.LSE_ABS
