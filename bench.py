@@ -47,6 +47,10 @@ def _args():
     ap.add_argument("--chunks", type=int, default=8, help="query-row blocks of the end-to-end pipeline")
     ap.add_argument("--only-index", action="store_true",
                     help="profiling aid: run kpool_build + dsa_index only (no q_lat / out allocation)")
+    ap.add_argument("--only-proj", action="store_true",
+                    help="profiling aid: run the absorbed-MLA projections only (mla_absorb_q, mla_v_proj)")
+    ap.add_argument("--d-nope", type=int, default=128, help="per-head key width of the absorbed projection")
+    ap.add_argument("--d-v", type=int, default=128, help="per-head value width of the V projection")
     return ap.parse_args()
 
 
@@ -247,6 +251,58 @@ def run_index_only(a, wl, inp, K, p, dev):
                       "status": K.check_status(layout.status)}))
 
 
+def run_proj(a, wl, K, dev, o_lat=None, flush=None):
+    """Times mla_absorb_q (q_nope -> q_lat) and mla_v_proj (o_lat -> o_v) on the workload's token count, 64
+    heads and d_nope/d_v from the flags.  Both are HBM-bound: the roofline is the algorithmic bytes (activations
+    in and out once, the weight once) over the measured copy bandwidth.  o_lat defaults to a seeded stand-in."""
+    import torch
+    from pooled_key_dsa_gb300 import workloads
+    dn, dv, H, T, D = a.d_nope, a.d_v, wl.n_heads, wl.T, wl.d_lat
+    q_nope_h, w_h = workloads.proj_inputs(wl, dn, dv)
+    q_nope, w = q_nope_h.to(dev), w_h.to(dev)
+    del q_nope_h
+    if o_lat is None:
+        o_lat = workloads.o_lat_input(wl).to(dev)
+    q_lat = torch.empty((T, H, D), dtype=torch.bfloat16, device=dev)
+    o_v = torch.empty((T, H, dv), dtype=torch.bfloat16, device=dev)
+    if flush is None:
+        flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+    evq, evv = [], []
+    for s in range(a.warmup + a.steps):
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        flush.zero_()
+        e[0].record(stream)
+        K.mla_absorb_q(q_nope, w, dn, dv, out=q_lat, status=status)
+        e[1].record(stream)
+        flush.zero_()
+        e[2].record(stream)
+        K.mla_v_proj(o_lat, w, dn, dv, out=o_v, status=status)
+        e[3].record(stream)
+        if s >= a.warmup:
+            evq.append((e[0], e[1]))
+            evv.append((e[2], e[3]))
+    torch.cuda.synchronize()
+    st = K.check_status(status)
+    q_ms = statistics.mean(x.elapsed_time(y) for x, y in evq)
+    v_ms = statistics.mean(x.elapsed_time(y) for x, y in evv)
+    w_bytes = H * (dn + dv) * D * 2
+    q_bytes = T * H * (dn + D) * 2 + H * dn * D * 2
+    v_bytes = T * H * (D + dv) * 2 + H * dv * D * 2
+    flops = 2.0 * T * H * D * dn, 2.0 * T * H * D * dv
+    hbm = _peaks()["hbm_gbs"]
+    res = {"d_nope": dn, "d_v": dv, "H": H, "T": T, "status": st,
+           "absorb_q": {"ms": q_ms, "GB/s": q_bytes / q_ms / 1e6, "frac": q_bytes / q_ms / 1e6 / hbm,
+                        "TFLOP/s": flops[0] / q_ms / 1e9, "algorithmic_bytes": q_bytes},
+           "v_proj": {"ms": v_ms, "GB/s": v_bytes / v_ms / 1e6, "frac": v_bytes / v_ms / 1e6 / hbm,
+                      "TFLOP/s": flops[1] / v_ms / 1e9, "algorithmic_bytes": v_bytes},
+           "bound": "hbm", "peak_gbs": hbm, "weight_bytes": w_bytes,
+           "what": "kv_b_proj absorbed into the query before the attention and applied to its output after"}
+    del q_nope, w, q_lat, o_v
+    return res
+
+
 # ----------------------------------------------------------------- our arm
 
 def main():
@@ -273,6 +329,10 @@ def main():
     K.lib()
 
     wl = workloads.workload(a.config)
+    if a.only_proj:
+        print(json.dumps({"mode": "proj_only", "config": _config(wl), "absorb": run_proj(a, wl, K,
+                                                                                         torch.device("cuda", local))}))
+        return
     inp = workloads.indexer_inputs(wl) if a.only_index else workloads.all_inputs(wl)
     dev = torch.device("cuda", local)
     p = K.make_params(topk=wl.topk, n_idx_heads=wl.n_idx_heads, d_idx=wl.d_idx, n_heads=wl.n_heads,
@@ -389,6 +449,8 @@ def main():
     torch.cuda.synchronize()
     is_ms = statistics.mean(x.elapsed_time(y) for x, y in is_ev)
     del q1, kv1, out1, lse1
+    # ---- the absorbed-MLA projections either side of the attention (V projection of this step's output)
+    proj = run_proj(a, wl, K, dev, o_lat=out, flush=flush)
     e2e_ms = sum(x.elapsed_time(y) for x, y in e2e_ev)
     tm = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
     if world > 1:
@@ -432,6 +494,7 @@ def main():
         "gpu_launches": LAUNCHES_PER_STEP * a.steps,
         "indexshare_layer": {"ms": is_ms, "tokens_per_s": T / (is_ms / 1e3),
                              "what": "a shared DSA layer: sparse_mla_fwd only, on the index rows of the step"},
+        "absorb": proj,
         "wall_s_timed": wall,
     }
     if world == 1 and not a.no_cpu_baseline:

@@ -277,6 +277,35 @@ int kpool_stage_select(const float* scores, const int64_t* pair_base, const kpoo
 typedef struct CUevent_st* kpool_event_t;
 int kpool_set_stage_events(kpool_event_t* events, int32_t n);
 
+/* ----------------------------------------------------------------------
+ * Absorbed-MLA projections either side of sparse_mla_fwd.
+ * NeMo AutoModel PR "add GLM-5.3-Flash training support", Changelog: the K
+ * projection is absorbed into the query, attention runs over the shared
+ * 512-wide latent, and the model-owned V projection follows.  miles
+ * "GLM-5.3-Flash" recipe, section 6 "LoRA RL": both use the kv_b_proj weight
+ * directly instead of calling that module.
+ *
+ *   w_kv_b  bf16 [n_heads*(d_nope+d_v), 512], the kv_b_proj weight stored
+ *           [out, in]: rows h*(d_nope+d_v) .. +d_nope-1 are head h's key
+ *           rows W_UK[h], the next d_v rows its value rows W_UV[h]
+ *   d_nope, d_v   64 or 128 each; n_heads 1..1024.  Other sizes return
+ *           KPOOL_ERR_SHAPE before any launch.
+ * Every pointer is a device pointer, 16-byte aligned (KPOOL_ERR_ALIGN).
+ * Results are bf16 (round to nearest even) of fp32 sums of exact bf16
+ * products.  T = 0 does nothing.  The only device error is KPOOL_ERR_TIMEOUT
+ * (a bounded wait that expired), recorded in *status (which may be NULL).
+ * ---------------------------------------------------------------------- */
+
+/* mla_absorb_q: q_lat[t,h,:] = sum_n q_nope[t,h,n] * W_UK[h][n,:].
+ *   q_nope  bf16 [T, n_heads, d_nope]   ->   q_lat  bf16 [T, n_heads, 512] */
+int mla_absorb_q(const void* q_nope, const void* w_kv_b, int32_t T, int32_t n_heads, int32_t d_nope,
+                 int32_t d_v, void* q_lat, int32_t* status, kpool_stream_t stream);
+
+/* mla_v_proj: o_v[t,h,:] = W_UV[h] . o_lat[t,h,:] (sum over the 512 latent).
+ *   o_lat   bf16 [T, n_heads, 512]      ->   o_v    bf16 [T, n_heads, d_v] */
+int mla_v_proj(const void* o_lat, const void* w_kv_b, int32_t T, int32_t n_heads, int32_t d_nope,
+               int32_t d_v, void* o_v, int32_t* status, kpool_stream_t stream);
+
 /* Synchronises `stream`, then returns the device status word's value (a
  * kpool_status), or KPOOL_ERR_CUDA if the stream or copy failed. */
 int kpool_check_status(const int32_t* status, kpool_stream_t stream);

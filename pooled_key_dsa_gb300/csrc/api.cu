@@ -143,6 +143,24 @@ int sparse_mla_fwd(const void* q_lat, const void* kv_lat, const int32_t* indices
     return sparse_mla_fwd_rows(q_lat, kv_lat, indices, W, T, T, n_heads, scale, out, lse, status, stream);
 }
 
+int mla_absorb_q(const void* q_nope, const void* w_kv_b, int32_t T, int32_t n_heads, int32_t d_nope, int32_t d_v,
+                 void* q_lat, int32_t* status, kpool_stream_t stream) {
+    if (T < 0 || !mla_proj_shape_ok(n_heads, d_nope, d_v)) return KPOOL_ERR_SHAPE;
+    if (T > 0 && (!q_nope || !w_kv_b || !q_lat)) return KPOOL_ERR_INVALID_ARG;
+    if (!aligned(q_nope, 16) || !aligned(w_kv_b, 16) || !aligned(q_lat, 16)) return KPOOL_ERR_ALIGN;
+    return launch_mla_proj(true, q_nope, w_kv_b, T, n_heads, d_nope, d_v, q_lat, status,
+                           reinterpret_cast<cudaStream_t>(stream));
+}
+
+int mla_v_proj(const void* o_lat, const void* w_kv_b, int32_t T, int32_t n_heads, int32_t d_nope, int32_t d_v,
+               void* o_v, int32_t* status, kpool_stream_t stream) {
+    if (T < 0 || !mla_proj_shape_ok(n_heads, d_nope, d_v)) return KPOOL_ERR_SHAPE;
+    if (T > 0 && (!o_lat || !w_kv_b || !o_v)) return KPOOL_ERR_INVALID_ARG;
+    if (!aligned(o_lat, 16) || !aligned(w_kv_b, 16) || !aligned(o_v, 16)) return KPOOL_ERR_ALIGN;
+    return launch_mla_proj(false, o_lat, w_kv_b, T, n_heads, d_nope, d_v, o_v, status,
+                           reinterpret_cast<cudaStream_t>(stream));
+}
+
 int kpool_forward_host(const kpool_host_io* h, const kpool_dev_io* d, int32_t n_docs, int32_t T,
                        const kpool_params* p, int32_t n_chunks, kpool_stream_t s_in, kpool_stream_t s_compute,
                        kpool_stream_t s_out) {
@@ -272,6 +290,6 @@ const char* kpool_strerror(int code) {
 
 // The tags after the arch name identify the kernel generations (used to match
 // stored profiler counters to the code that produced them).
-const char* kpool_version(void) { return "kpooldsa 0.3 sm_103a mla-tc5 score-tc1 select2"; }
+const char* kpool_version(void) { return "kpooldsa 0.4 sm_103a mla-tc5 score-tc1 select2 proj1"; }
 
 }  // extern "C"

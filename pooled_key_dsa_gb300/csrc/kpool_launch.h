@@ -52,4 +52,9 @@ int launch_sparse_mla(const uint16_t* q_lat, const uint16_t* kv_lat, const int32
                       int T, int n_heads, float scale, uint16_t* out, float* lse, int32_t* status,
                       cudaStream_t stream);
 
+// Absorbed-MLA projections (absorb: q_nope -> q_lat; otherwise o_lat -> o_v).
+bool mla_proj_shape_ok(int n_heads, int d_nope, int d_v);
+int launch_mla_proj(bool absorb, const void* act, const void* w_kv_b, int T, int n_heads, int d_nope, int d_v,
+                    void* out, int32_t* status, cudaStream_t stream);
+
 }  // namespace kpool

@@ -26,6 +26,7 @@
 #include "kpool_common.cuh"
 #include "kpool_launch.h"
 #include "tc_ptx.cuh"
+#include "tmap_host.h"
 
 namespace kpool {
 
@@ -278,23 +279,10 @@ int scoring_group(int n_idx_heads, int d_idx) {
     }
 }
 
-static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    if (!fn) {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    }
-    return fn;
-}
-
 // 2-D byte tensor [rows, 128] with 128-byte rows, 128-byte swizzle, box
 // {128, box_rows}.
 static bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows) {
-    auto fn = encode_fn();
+    auto fn = tensor_map_encoder();
     if (!fn) return false;
     const cuuint64_t dims[2] = {128, rows};
     const cuuint64_t strides[1] = {128};

@@ -22,7 +22,7 @@ CODES = {v: k for k, v in ERRORS.items()}
 
 EXPORTED = ("kpool_workspace_bytes", "kpool_workspace_offsets", "kpool_build", "dsa_index", "sparse_mla_fwd",
             "kpool_stage_select", "kpool_set_stage_events", "kpool_check_status", "kpool_strerror", "kpool_version",
-            "dsa_index_noalloc", "sparse_mla_fwd_rows", "kpool_forward_host")
+            "dsa_index_noalloc", "sparse_mla_fwd_rows", "kpool_forward_host", "mla_absorb_q", "mla_v_proj")
 
 
 class KpoolUnavailable(ImportError):
@@ -87,6 +87,8 @@ def lib():
         L.sparse_mla_fwd_rows.argtypes = [vp, vp, vp, i32, i32, i32, i32, ctypes.c_float, vp, vp, vp, vp]
         L.kpool_forward_host.argtypes = [ctypes.POINTER(HostIO), ctypes.POINTER(DevIO), i32, i32,
                                          ctypes.POINTER(Params), i32, vp, vp, vp]
+        L.mla_absorb_q.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp]
+        L.mla_v_proj.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp]
         L.kpool_stage_select.argtypes = [vp, vp, ctypes.POINTER(LayoutC), i32, vp, i32, vp]
         L.dsa_index_noalloc.argtypes = [vp, vp, vp, ctypes.POINTER(LayoutC), i32, ctypes.POINTER(Params), vp, i32,
                                         vp]
@@ -262,6 +264,40 @@ def sparse_mla_fwd_rows(q_lat, kv_lat, indices, scale: float, out=None, lse=None
                                      float(scale), _ptr(out), _ptr(lse), _ptr(status), _stream(stream)),
            "sparse_mla_fwd_rows")
     return out, lse
+
+
+def _proj_weight(w_kv_b, H: int, d_nope: int, d_v: int, D: int):
+    _want(w_kv_b, torch.bfloat16, (H * (d_nope + d_v), D), "w_kv_b")
+
+
+def mla_absorb_q(q_nope, w_kv_b, d_nope: int, d_v: int, out=None, status=None, stream=None):
+    """Query absorption: q_lat[t,h,:] = q_nope[t,h,:] . W_UK[h] with W_UK[h] the d_nope key rows of head h in the
+    kv_b_proj weight w_kv_b [H*(d_nope+d_v), 512].  q_nope [T, H, d_nope] bf16 -> q_lat [T, H, 512] bf16."""
+    T, H, dn = q_nope.shape
+    if dn != d_nope:
+        raise ValueError("q_nope's last dimension must be d_nope")
+    _want(q_nope, torch.bfloat16, (T, H, dn), "q_nope")
+    _proj_weight(w_kv_b, H, d_nope, d_v, 512)
+    if out is None:
+        out = torch.empty((T, H, 512), dtype=torch.bfloat16, device=q_nope.device)
+    _want(out, torch.bfloat16, (T, H, 512), "q_lat")
+    _check(lib().mla_absorb_q(_ptr(q_nope), _ptr(w_kv_b), T, H, d_nope, d_v, _ptr(out), _ptr(status),
+                              _stream(stream)), "mla_absorb_q")
+    return out
+
+
+def mla_v_proj(o_lat, w_kv_b, d_nope: int, d_v: int, out=None, status=None, stream=None):
+    """V projection: o_v[t,h,:] = W_UV[h] . o_lat[t,h,:] with W_UV[h] the d_v value rows of head h in the
+    kv_b_proj weight.  o_lat [T, H, 512] bf16 -> o_v [T, H, d_v] bf16."""
+    T, H, D = o_lat.shape
+    _want(o_lat, torch.bfloat16, (T, H, 512), "o_lat")
+    _proj_weight(w_kv_b, H, d_nope, d_v, D)
+    if out is None:
+        out = torch.empty((T, H, d_v), dtype=torch.bfloat16, device=o_lat.device)
+    _want(out, torch.bfloat16, (T, H, d_v), "o_v")
+    _check(lib().mla_v_proj(_ptr(o_lat), _ptr(w_kv_b), T, H, d_nope, d_v, _ptr(out), _ptr(status),
+                            _stream(stream)), "mla_v_proj")
+    return out
 
 
 _HOST_KEYS = ("k", "gate", "ape", "cu_seqlens", "q_idx", "w", "q_lat", "kv_lat", "out", "lse")

@@ -193,6 +193,25 @@ def layer_attention_inputs(wl: Workload, layer: int, rows=None) -> tuple:
     return q, kv
 
 
+# tensor ids of the absorbed-MLA projection inputs
+_QNOPE, _WKVB, _OLAT = 8, 9, 10
+
+
+def proj_inputs(wl: Workload, d_nope: int = 128, d_v: int = 128, rows=None) -> tuple:
+    """(q_nope bf16 [T, H, d_nope] or the given token rows of it, w_kv_b bf16 [H*(d_nope+d_v), D]).
+    q_nope is N(0,1); the kv_b_proj weight is N(0,1)/sqrt(D), so that a projected latent row has about
+    unit variance."""
+    H, D = wl.n_heads, wl.d_lat
+    q_nope = _chunked_bf16(wl.seed, _QNOPE, wl.T, (H, d_nope), rows=rows)
+    w = _bf16(_normal(wl.seed, _WKVB, (H * (d_nope + d_v), D)) / np.float32(math.sqrt(D)))
+    return q_nope, w
+
+
+def o_lat_input(wl: Workload, rows=None) -> torch.Tensor:
+    """A stand-in latent attention output, bf16 [T, H, D] N(0,1), for the V projection on its own."""
+    return _chunked_bf16(wl.seed, _OLAT, wl.T, (wl.n_heads, wl.d_lat), rows=rows)
+
+
 def all_inputs(wl: Workload) -> Inputs:
     inp = indexer_inputs(wl)
     inp.q_lat = q_lat(wl)

@@ -116,6 +116,18 @@ def test_host_checks_of_the_row_block_and_host_pipeline_entries(lib):
                                   None) == K.CODES["KPOOL_ERR_INVALID_ARG"]     # layout T differs
 
 
+def test_host_checks_of_the_projection_entries(lib):
+    vp = ctypes.c_void_p
+    for fn in (lib.mla_absorb_q, lib.mla_v_proj):
+        # unsupported widths and head counts are refused before any launch
+        for dn, dv, H in ((96, 128, 64), (128, 256, 64), (128, 128, 0), (0, 64, 4)):
+            assert fn(vp(16), vp(16), 64, H, dn, dv, vp(16), None, None) == K.CODES["KPOOL_ERR_SHAPE"]
+        assert fn(vp(16), vp(16), -1, 64, 128, 128, vp(16), None, None) == K.CODES["KPOOL_ERR_SHAPE"]
+        assert fn(None, vp(16), 64, 64, 128, 128, vp(16), None, None) == K.CODES["KPOOL_ERR_INVALID_ARG"]
+        assert fn(vp(16), vp(24), 64, 64, 128, 128, vp(16), None, None) == K.CODES["KPOOL_ERR_ALIGN"]
+        assert fn(None, None, 0, 64, 128, 128, None, None, None) == K.KPOOL_OK        # T = 0: nothing to do
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(K, "_lib", None)
     monkeypatch.setattr(K, "_LIB_PATH", str(tmp_path / "missing.so"))
