@@ -32,7 +32,9 @@ Readings where the pages are silent (each one a parameter or a stated choice):
   * when (r+1) % 4 == 0 the query's own pool is complete and only competes in
     the top-k, so the own tail holds (r+1) % 4 <= 3 tokens (2048 + 3 = 2051);
   * index rows list the valid positions in ascending order, then -1;
-  * attention scale is a parameter (1/sqrt(512)); LSE is the natural log.
+  * attention scale is a parameter (1/sqrt(512)); LSE is the natural log;
+  * the backward (section 9) is the exact gradient of that attention, with
+    the latent row as both key and value (its gradient sums both roles).
 
 Every floating-point step is float64 unless a step says fp32, in which case it
 is np.float32 arithmetic in the same order as written here.
@@ -323,3 +325,49 @@ def indexer(q_idx, k, gate, ape, w, cu_seqlens, topk, W, rows=None, kpool=KPOOL,
     if with_scores:
         res["scores"] = S
     return res
+
+
+# ----------------------------------------------------------------- 9. attention backward
+
+def sparse_attention_bwd(q_lat, kv_lat, indices, scale, dout, rows, T=None) -> dict:
+    """Gradients of the absorbed sparse latent attention [PR3699] for the given
+    query rows, given dL/dout.  The latent row kv[j] is both key and value, so
+    it collects a value term and a key term.  Float64, per query i and head h,
+    over the valid slots j of the row:
+        p_j   = softmax(scale * q[i,h] . kv[j])
+        dp_j  = dout[i,h] . kv[j]
+        delta = sum_j p_j dp_j             (= dout[i,h] . out[i,h])
+        dz_j  = p_j (dp_j - delta)
+        dq[i,h] = scale * sum_j dz_j kv[j]
+        dkv[j] += p_j dout[i,h] + scale * dz_j q[i,h]
+    ``q_lat``/``dout`` are indexed by position in ``rows``; dkv [T, D] holds the
+    contributions of these rows only.  Returns dq [len(rows),H,D], dkv [T,D],
+    and the recomputed out [len(rows),H,D] and lse [len(rows),H] (float64)."""
+    q_lat = np.asarray(q_lat, dtype=np.float64)
+    dout = np.asarray(dout, dtype=np.float64)
+    kv_all = np.asarray(kv_lat, dtype=np.float64)
+    T = kv_all.shape[0] if T is None else T
+    n, H, D = q_lat.shape
+    dq = np.zeros((n, H, D))
+    dkv = np.zeros((T, D))
+    out = np.zeros((n, H, D))
+    lse = np.full((n, H), -np.inf)
+    for m in range(n):
+        idx = np.asarray(indices[m])
+        valid = idx[idx >= 0]
+        if len(valid) == 0:
+            continue
+        kv = kv_all[valid]                                  # [n_v, D]
+        z = float(scale) * (q_lat[m] @ kv.T)                # [H, n_v]
+        zmax = z.max(axis=1, keepdims=True)
+        e = np.exp(z - zmax)
+        s = e.sum(axis=1, keepdims=True)
+        p = e / s
+        out[m] = p @ kv
+        lse[m] = zmax[:, 0] + np.log(s[:, 0])
+        dp = dout[m] @ kv.T                                 # [H, n_v]
+        delta = (dout[m] * out[m]).sum(axis=1, keepdims=True)
+        dz = p * (dp - delta)
+        dq[m] = float(scale) * (dz @ kv)
+        np.add.at(dkv, valid, p.T @ dout[m] + float(scale) * (dz.T @ q_lat[m]))
+    return {"dq": dq, "dkv": dkv, "out": out, "lse": lse}
