@@ -49,6 +49,8 @@ def _args():
                     help="profiling aid: run kpool_build + dsa_index only (no q_lat / out allocation)")
     ap.add_argument("--only-proj", action="store_true",
                     help="profiling aid: run the absorbed-MLA projections only (mla_absorb_q, mla_v_proj)")
+    ap.add_argument("--only-bwd", action="store_true",
+                    help="profiling aid: index rows and the forward once, then time sparse_mla_bwd only")
     ap.add_argument("--d-nope", type=int, default=128, help="per-head key width of the absorbed projection")
     ap.add_argument("--d-v", type=int, default=128, help="per-head value width of the V projection")
     return ap.parse_args()
@@ -303,6 +305,61 @@ def run_proj(a, wl, K, dev, o_lat=None, flush=None):
     return res
 
 
+def run_bwd(a, wl, K, dev, q, kv, idx, out, lse, valid_slots, flush):
+    """Times sparse_mla_bwd on the step's index rows and forward results with a seeded dout.  Its bound is the
+    fp32 reduction of dKv into L2 (2 KB per valid slot), whose rate is measured here as well with the same access
+    pattern (kpool_measure_l2_reduce over random rows of a [T, 512] fp32 buffer); the tensor work is
+    5 GEMM terms of 2*H*D FLOP per valid slot (S, dP, dQ, and the two of dKv)."""
+    import torch
+    from pooled_key_dsa_gb300 import workloads
+    T, H, D = wl.T, wl.n_heads, wl.d_lat
+    dout = workloads.dout_input(wl).to(dev)
+    dq = torch.empty_like(q)
+    dkv = torch.empty((T, D), dtype=torch.float32, device=dev)
+    delta = torch.empty((T, H), dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream()
+    ev = []
+    for s in range(a.warmup + a.steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        K.sparse_mla_bwd(q, kv, idx, wl.scale, out, lse, dout, dq=dq, dkv=dkv, delta=delta, status=status)
+        e1.record(stream)
+        if s >= a.warmup:
+            ev.append((e0, e1))
+    torch.cuda.synchronize()
+    st = K.check_status(status)
+    ms = statistics.mean(x.elapsed_time(y) for x, y in ev)
+    # reduction rate with the same access pattern: 2^21 random rows of 2 KB into a [T, 512] fp32 buffer
+    buf = torch.zeros((T, D), dtype=torch.float32, device=dev)
+    g = torch.Generator(device="cpu").manual_seed(1234)
+    ids = torch.randint(0, T, (1 << 21,), generator=g, dtype=torch.int32).to(dev)
+    rev = []
+    for s in range(a.warmup + a.steps):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        K.measure_l2_reduce(buf, ids)
+        e1.record(stream)
+        if s >= a.warmup:
+            rev.append((e0, e1))
+    torch.cuda.synchronize()
+    r_ms = statistics.mean(x.elapsed_time(y) for x, y in rev)
+    red_peak = ids.numel() * D * 4 / r_ms / 1e6
+    red_bytes = valid_slots * D * 4
+    achieved = red_bytes / ms / 1e6
+    flops = 5 * 2.0 * H * D * valid_slots
+    del dout, dq, dkv, delta, buf, ids
+    return {"ms": ms, "tokens_per_s": T / (ms / 1e3), "status": st,
+            "roofline": {"bound": "l2_reduce", "achieved": achieved, "peak": red_peak, "unit": "GB/s",
+                         "frac": achieved / red_peak, "traffic": None,
+                         "peak_kind": "measured in this run: kpool_measure_l2_reduce, 2^21 random 2 KB rows",
+                         "algorithmic": f"valid_slots*512*4 = {red_bytes:.4e} B of fp32 reductions per launch"},
+            "tensor_tflops": flops / ms / 1e9,
+            "tensor_algorithmic": f"5*2*H*D*valid_slots = {flops:.4e} FLOP per launch",
+            "what": "sparse_mla_bwd (delta, dQ, dKV) on the step's index rows and forward results, seeded dout"}
+
+
 # ----------------------------------------------------------------- our arm
 
 def main():
@@ -341,6 +398,18 @@ def main():
 
     if a.only_index:
         run_index_only(a, wl, inp, K, p, dev)
+        return
+    if a.only_bwd:
+        d = {"cu_seqlens": torch.from_numpy(inp.cu_seqlens).to(dev), "q_idx": inp.q_idx.to(dev), "k": inp.k.to(dev),
+             "gate": torch.from_numpy(inp.gate).to(dev), "ape": torch.from_numpy(inp.ape).to(dev),
+             "w": torch.from_numpy(inp.w).to(dev), "q_lat": inp.q_lat.to(dev), "kv_lat": inp.kv_lat.to(dev)}
+        kp, lay = K.kpool_build(d["k"], d["gate"], d["ape"], d["cu_seqlens"], p)
+        idx = K.dsa_index(d["q_idx"], d["w"], kp, lay, wl.topk, p, W=W)
+        out, lse = K.sparse_mla_fwd(d["q_lat"], d["kv_lat"], idx, wl.scale, status=lay.status)
+        flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+        res = run_bwd(a, wl, K, dev, d["q_lat"], d["kv_lat"], idx, out, lse, _work(wl)["valid_slots"], flush)
+        print(json.dumps({"mode": "bwd_only", "config": _config(wl), "sparse_mla_bwd": res,
+                          "status": K.check_status(lay.status)}))
         return
     host = {"cu_seqlens": torch.from_numpy(inp.cu_seqlens), "q_idx": inp.q_idx, "k": inp.k,
             "gate": torch.from_numpy(inp.gate), "ape": torch.from_numpy(inp.ape), "w": torch.from_numpy(inp.w),
@@ -451,6 +520,8 @@ def main():
     del q1, kv1, out1, lse1
     # ---- the absorbed-MLA projections either side of the attention (V projection of this step's output)
     proj = run_proj(a, wl, K, dev, o_lat=out, flush=flush)
+    # ---- the backward of the attention on this step's rows and results
+    bwd = run_bwd(a, wl, K, dev, d["q_lat"], d["kv_lat"], idx, out, lse, _work(wl)["valid_slots"], flush)
     e2e_ms = sum(x.elapsed_time(y) for x, y in e2e_ev)
     tm = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
     if world > 1:
@@ -495,6 +566,7 @@ def main():
         "indexshare_layer": {"ms": is_ms, "tokens_per_s": T / (is_ms / 1e3),
                              "what": "a shared DSA layer: sparse_mla_fwd only, on the index rows of the step"},
         "absorb": proj,
+        "sparse_mla_bwd": bwd,
         "wall_s_timed": wall,
     }
     if world == 1 and not a.no_cpu_baseline:

@@ -277,6 +277,42 @@ int kpool_stage_select(const float* scores, const int64_t* pair_base, const kpoo
 typedef struct CUevent_st* kpool_event_t;
 int kpool_set_stage_events(kpool_event_t* events, int32_t n);
 
+/* sparse_mla_bwd: gradients of sparse_mla_fwd.
+ * NeMo AutoModel PR "add GLM-5.3-Flash training support", Changelog and
+ * "cuDNN sparse MLA parity and performance": training runs the latent sparse
+ * attention backward for dQ and dKV.  The latent row is both key and value,
+ * so dkv sums a value term and a key term.  Per query i, head h, over the
+ * valid slots j of row i (p the forward's softmax, rebuilt from lse):
+ *   delta = dout[i,h] . out[i,h]
+ *   dz_j  = p_j * (dout[i,h] . kv[j] - delta)
+ *   dq[i,h]  = scale * sum_j dz_j kv[j]
+ *   dkv[j]  += p_j dout[i,h] + scale * dz_j q[i,h]
+ *   q_lat, kv_lat, indices, W, T, n_heads, scale: as for sparse_mla_fwd
+ *   out     bf16 [T, n_heads, 512]  and  lse fp32 [T, n_heads]: the forward's
+ *           results for these inputs
+ *   dout    bf16 [T, n_heads, 512]  gradient of the loss w.r.t. out
+ *   dq      bf16 [T, n_heads, 512]  written (rows with no valid slot: 0)
+ *   dkv     fp32 [T, 512]           overwritten: zeroed by the call, then
+ *           accumulated with fp32 atomic reductions, so the summation order
+ *           (and the last bits) can differ between calls
+ *   delta   fp32 [T, n_heads]       caller-allocated scratch, written
+ * Alignment: q_lat, kv_lat, out, dout, dq, dkv 16 bytes; indices, lse, delta
+ * 4 bytes.  Index entries outside [-1, T) are skipped and recorded as
+ * KPOOL_ERR_INDEX_RANGE; KPOOL_ERR_TIMEOUT as for the forward. */
+int sparse_mla_bwd(const void* q_lat, const void* kv_lat, const int32_t* indices, int32_t W, int32_t T,
+                   int32_t n_heads, float scale, const void* out, const float* lse, const void* dout, void* dq,
+                   float* dkv, float* delta, int32_t* status, kpool_stream_t stream);
+
+/* kpool_measure_l2_reduce: measurement utility, no counterpart on the pages.
+ * Adds 1.0f to each of the 512 floats of rows buf[row_ids[k]], k < n_ids,
+ * with fp32 reductions in sparse_mla_bwd's dkv access pattern (each warp
+ * instruction covers 128 contiguous bytes of one row), so that a caller can
+ * time the reduction rate that bounds sparse_mla_bwd.
+ *   buf      fp32 [rows, 512], device, 16-byte aligned
+ *   row_ids  int32 [n_ids], device; ids outside [0, rows) are skipped */
+int kpool_measure_l2_reduce(float* buf, int32_t rows, const int32_t* row_ids, int32_t n_ids,
+                            kpool_stream_t stream);
+
 /* ----------------------------------------------------------------------
  * Absorbed-MLA projections either side of sparse_mla_fwd.
  * NeMo AutoModel PR "add GLM-5.3-Flash training support", Changelog: the K

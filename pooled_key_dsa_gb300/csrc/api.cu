@@ -143,6 +143,31 @@ int sparse_mla_fwd(const void* q_lat, const void* kv_lat, const int32_t* indices
     return sparse_mla_fwd_rows(q_lat, kv_lat, indices, W, T, T, n_heads, scale, out, lse, status, stream);
 }
 
+int sparse_mla_bwd(const void* q_lat, const void* kv_lat, const int32_t* indices, int32_t W, int32_t T,
+                   int32_t n_heads, float scale, const void* out, const float* lse, const void* dout, void* dq,
+                   float* dkv, float* delta, int32_t* status, kpool_stream_t stream) {
+    if (T < 0 || W < 1 || n_heads < 1 || n_heads > 64) return KPOOL_ERR_SHAPE;
+    if (T > 0 && (!q_lat || !kv_lat || !indices || !out || !lse || !dout || !dq || !dkv || !delta))
+        return KPOOL_ERR_INVALID_ARG;
+    if (!aligned(q_lat, 16) || !aligned(kv_lat, 16) || !aligned(out, 16) || !aligned(dout, 16) || !aligned(dq, 16) ||
+        !aligned(dkv, 16) || !aligned(indices, 4) || !aligned(lse, 4) || !aligned(delta, 4))
+        return KPOOL_ERR_ALIGN;
+    if (!(scale == scale)) return KPOOL_ERR_INVALID_ARG;
+    if (T == 0) return KPOOL_OK;
+    return launch_sparse_mla_bwd(static_cast<const uint16_t*>(q_lat), static_cast<const uint16_t*>(kv_lat), indices,
+                                 W, T, T, n_heads, scale, static_cast<const uint16_t*>(out), lse,
+                                 static_cast<const uint16_t*>(dout), static_cast<uint16_t*>(dq), dkv, delta, status,
+                                 reinterpret_cast<cudaStream_t>(stream));
+}
+
+int kpool_measure_l2_reduce(float* buf, int32_t rows, const int32_t* row_ids, int32_t n_ids,
+                            kpool_stream_t stream) {
+    if (rows < 0 || n_ids < 0) return KPOOL_ERR_SHAPE;
+    if (n_ids > 0 && (!buf || !row_ids)) return KPOOL_ERR_INVALID_ARG;
+    if (!aligned(buf, 16) || !aligned(row_ids, 4)) return KPOOL_ERR_ALIGN;
+    return launch_l2_reduce(buf, rows, row_ids, n_ids, reinterpret_cast<cudaStream_t>(stream));
+}
+
 int mla_absorb_q(const void* q_nope, const void* w_kv_b, int32_t T, int32_t n_heads, int32_t d_nope, int32_t d_v,
                  void* q_lat, int32_t* status, kpool_stream_t stream) {
     if (T < 0 || !mla_proj_shape_ok(n_heads, d_nope, d_v)) return KPOOL_ERR_SHAPE;
@@ -290,6 +315,6 @@ const char* kpool_strerror(int code) {
 
 // The tags after the arch name identify the kernel generations (used to match
 // stored profiler counters to the code that produced them).
-const char* kpool_version(void) { return "kpooldsa 0.4 sm_103a mla-tc5 score-tc1 select2 proj1"; }
+const char* kpool_version(void) { return "kpooldsa 0.5 sm_103a mla-tc5 score-tc1 select2 proj1 bwd3"; }
 
 }  // extern "C"

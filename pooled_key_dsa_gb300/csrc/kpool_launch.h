@@ -52,6 +52,16 @@ int launch_sparse_mla(const uint16_t* q_lat, const uint16_t* kv_lat, const int32
                       int T, int n_heads, float scale, uint16_t* out, float* lse, int32_t* status,
                       cudaStream_t stream);
 
+// Sparse latent attention backward: zeroes dkv, computes delta = rowsum(out * dout) into `delta`
+// [n_rows, H], then dq (bf16) and dkv (fp32 reductions).
+int launch_sparse_mla_bwd(const uint16_t* q_lat, const uint16_t* kv_lat, const int32_t* indices, int W, int n_rows,
+                          int T, int n_heads, float scale, const uint16_t* out, const float* lse,
+                          const uint16_t* dout, uint16_t* dq, float* dkv, float* delta, int32_t* status,
+                          cudaStream_t stream);
+
+// Measurement: fp32 reductions into 512-float rows (the dKv scatter's access pattern).
+int launch_l2_reduce(float* buf, int rows, const int32_t* row_ids, int n_ids, cudaStream_t stream);
+
 // Absorbed-MLA projections (absorb: q_nope -> q_lat; otherwise o_lat -> o_v).
 bool mla_proj_shape_ok(int n_heads, int d_nope, int d_v);
 int launch_mla_proj(bool absorb, const void* act, const void* w_kv_b, int T, int n_heads, int d_nope, int d_v,

@@ -22,7 +22,8 @@ CODES = {v: k for k, v in ERRORS.items()}
 
 EXPORTED = ("kpool_workspace_bytes", "kpool_workspace_offsets", "kpool_build", "dsa_index", "sparse_mla_fwd",
             "kpool_stage_select", "kpool_set_stage_events", "kpool_check_status", "kpool_strerror", "kpool_version",
-            "dsa_index_noalloc", "sparse_mla_fwd_rows", "kpool_forward_host", "mla_absorb_q", "mla_v_proj")
+            "dsa_index_noalloc", "sparse_mla_fwd_rows", "kpool_forward_host", "mla_absorb_q", "mla_v_proj",
+            "sparse_mla_bwd", "kpool_measure_l2_reduce")
 
 
 class KpoolUnavailable(ImportError):
@@ -87,6 +88,8 @@ def lib():
         L.sparse_mla_fwd_rows.argtypes = [vp, vp, vp, i32, i32, i32, i32, ctypes.c_float, vp, vp, vp, vp]
         L.kpool_forward_host.argtypes = [ctypes.POINTER(HostIO), ctypes.POINTER(DevIO), i32, i32,
                                          ctypes.POINTER(Params), i32, vp, vp, vp]
+        L.sparse_mla_bwd.argtypes = [vp, vp, vp, i32, i32, i32, ctypes.c_float, vp, vp, vp, vp, vp, vp, vp, vp]
+        L.kpool_measure_l2_reduce.argtypes = [vp, i32, vp, i32, vp]
         L.mla_absorb_q.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp]
         L.mla_v_proj.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp]
         L.kpool_stage_select.argtypes = [vp, vp, ctypes.POINTER(LayoutC), i32, vp, i32, vp]
@@ -264,6 +267,46 @@ def sparse_mla_fwd_rows(q_lat, kv_lat, indices, scale: float, out=None, lse=None
                                      float(scale), _ptr(out), _ptr(lse), _ptr(status), _stream(stream)),
            "sparse_mla_fwd_rows")
     return out, lse
+
+
+def sparse_mla_bwd(q_lat, kv_lat, indices, scale: float, out, lse, dout, dq=None, dkv=None, delta=None,
+                   status=None, stream=None):
+    """Gradients of sparse_mla_fwd: returns (dq bf16 [T, H, 512], dkv fp32 [T, 512]).  out and lse are the
+    forward's results; dout is dL/dout.  dkv is accumulated with fp32 atomics (its last bits depend on the
+    order in which they land)."""
+    T, H, D = q_lat.shape
+    _want(q_lat, torch.bfloat16, (T, H, D), "q_lat")
+    _want(kv_lat, torch.bfloat16, (T, D), "kv_lat")
+    _want(indices, torch.int32, None, "indices")
+    if indices.dim() != 2 or indices.shape[0] != T:
+        raise ValueError("indices must be [T, W]")
+    _want(out, torch.bfloat16, (T, H, D), "out")
+    _want(lse, torch.float32, (T, H), "lse")
+    _want(dout, torch.bfloat16, (T, H, D), "dout")
+    if dq is None:
+        dq = torch.empty_like(q_lat)
+    if dkv is None:
+        dkv = torch.empty((T, D), dtype=torch.float32, device=q_lat.device)
+    if delta is None:
+        delta = torch.empty((T, H), dtype=torch.float32, device=q_lat.device)
+    _want(dq, torch.bfloat16, (T, H, D), "dq")
+    _want(dkv, torch.float32, (T, D), "dkv")
+    _want(delta, torch.float32, (T, H), "delta")
+    _check(lib().sparse_mla_bwd(_ptr(q_lat), _ptr(kv_lat), _ptr(indices), indices.shape[1], T, H, float(scale),
+                                _ptr(out), _ptr(lse), _ptr(dout), _ptr(dq), _ptr(dkv), _ptr(delta), _ptr(status),
+                                _stream(stream)), "sparse_mla_bwd")
+    return dq, dkv
+
+
+def measure_l2_reduce(buf, row_ids, stream=None):
+    """Adds 1.0 to every element of the rows buf[row_ids] (fp32 [rows, 512]) with the dkv scatter's fp32
+    reductions; a timing aid for the reduction rate that bounds sparse_mla_bwd."""
+    _want(buf, torch.float32, None, "buf")
+    _want(row_ids, torch.int32, None, "row_ids")
+    if buf.dim() != 2 or buf.shape[1] != 512:
+        raise ValueError("buf must be [rows, 512]")
+    _check(lib().kpool_measure_l2_reduce(_ptr(buf), buf.shape[0], _ptr(row_ids), row_ids.numel(), _stream(stream)),
+           "kpool_measure_l2_reduce")
 
 
 def _proj_weight(w_kv_b, H: int, d_nope: int, d_v: int, D: int):

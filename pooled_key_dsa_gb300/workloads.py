@@ -193,8 +193,8 @@ def layer_attention_inputs(wl: Workload, layer: int, rows=None) -> tuple:
     return q, kv
 
 
-# tensor ids of the absorbed-MLA projection inputs
-_QNOPE, _WKVB, _OLAT = 8, 9, 10
+# tensor ids of the absorbed-MLA projection inputs and of the attention's output gradient
+_QNOPE, _WKVB, _OLAT, _DOUT = 8, 9, 10, 11
 
 
 def proj_inputs(wl: Workload, d_nope: int = 128, d_v: int = 128, rows=None) -> tuple:
@@ -210,6 +210,11 @@ def proj_inputs(wl: Workload, d_nope: int = 128, d_v: int = 128, rows=None) -> t
 def o_lat_input(wl: Workload, rows=None) -> torch.Tensor:
     """A stand-in latent attention output, bf16 [T, H, D] N(0,1), for the V projection on its own."""
     return _chunked_bf16(wl.seed, _OLAT, wl.T, (wl.n_heads, wl.d_lat), rows=rows)
+
+
+def dout_input(wl: Workload, rows=None) -> torch.Tensor:
+    """A seeded gradient of the loss w.r.t. the attention output, bf16 [T, H, D] N(0,1)."""
+    return _chunked_bf16(wl.seed, _DOUT, wl.T, (wl.n_heads, wl.d_lat), rows=rows)
 
 
 def all_inputs(wl: Workload) -> Inputs:

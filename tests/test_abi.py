@@ -128,6 +128,28 @@ def test_host_checks_of_the_projection_entries(lib):
         assert fn(None, None, 0, 64, 128, 128, None, None, None) == K.KPOOL_OK        # T = 0: nothing to do
 
 
+def test_host_checks_of_the_backward_entry(lib):
+    vp = ctypes.c_void_p
+    ok = [vp(16)] * 3
+    bwd = lib.sparse_mla_bwd
+    assert bwd(*ok, 128, 64, 65, 0.1, vp(16), vp(16), vp(16), vp(16), vp(16), vp(16), None,
+               None) == K.CODES["KPOOL_ERR_SHAPE"]                         # more than 64 heads
+    assert bwd(*ok, 0, 64, 64, 0.1, vp(16), vp(16), vp(16), vp(16), vp(16), vp(16), None,
+               None) == K.CODES["KPOOL_ERR_SHAPE"]                         # W < 1
+    assert bwd(*ok, 128, 64, 64, 0.1, vp(16), vp(16), None, vp(16), vp(16), vp(16), None,
+               None) == K.CODES["KPOOL_ERR_INVALID_ARG"]                   # dout missing
+    assert bwd(*ok, 128, 64, 64, 0.1, vp(16), vp(16), vp(16), vp(8), vp(16), vp(16), None,
+               None) == K.CODES["KPOOL_ERR_ALIGN"]                         # dq misaligned
+    assert bwd(*ok, 128, 64, 64, float("nan"), vp(16), vp(16), vp(16), vp(16), vp(16), vp(16), None,
+               None) == K.CODES["KPOOL_ERR_INVALID_ARG"]
+    assert bwd(None, None, None, 128, 0, 64, 0.1, None, None, None, None, None, None, None, None) == K.KPOOL_OK
+    red = lib.kpool_measure_l2_reduce
+    assert red(vp(16), -1, vp(16), 4, None) == K.CODES["KPOOL_ERR_SHAPE"]
+    assert red(None, 8, vp(16), 4, None) == K.CODES["KPOOL_ERR_INVALID_ARG"]
+    assert red(vp(8), 8, vp(16), 4, None) == K.CODES["KPOOL_ERR_ALIGN"]
+    assert red(None, 8, None, 0, None) == K.KPOOL_OK
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(K, "_lib", None)
     monkeypatch.setattr(K, "_LIB_PATH", str(tmp_path / "missing.so"))
