@@ -303,6 +303,56 @@ int sparse_mla_bwd(const void* q_lat, const void* kv_lat, const int32_t* indices
                    int32_t n_heads, float scale, const void* out, const float* lse, const void* dout, void* dq,
                    float* dkv, float* delta, int32_t* status, kpool_stream_t stream);
 
+/* ----------------------------------------------------------------------
+ * Paged decode.  prime-rl PR "GLM-5.3-Flash text model", section "Patches
+ * and workarounds": serving aligns hybrid KV blocks to index_kpool x 32 = 128
+ * tokens, and the paged indexer kernel takes pages of 32 pools on SM100.  One
+ * page id indexes three caches:
+ *   k8_cache  e4m3 [n_pages, 32, d_i]   pooled-key codes (16-byte aligned)
+ *   sk_cache  fp32 [n_pages, 32]        their per-vector scales
+ *   kv_cache  bf16 [n_pages, 128, 512]  latent rows (read by sparse_mla_fwd_rows)
+ *   block_table int32 [B, max_pages]: page of tokens 128j .. 128j+127 of sequence b
+ * Sizes: d_i = 128, n_idx_heads 16 or 32, kpool 4 (else KPOOL_ERR_SHAPE).
+ * Pooling, Hadamard, FP8, scoring, top-k and row rules are those of
+ * kpool_build / dsa_index; a sequence is one document.
+ * ---------------------------------------------------------------------- */
+
+/* kpool_paged_append: pooled keys into the page cache.  For item v, the pool
+ * of the 4 token rows pool_tok[v] .. pool_tok[v]+3 of k (bf16 [*, d_i]) and
+ * gate (fp32 [*, d_i]) with ape (fp32 [4, d_i]) is Hadamard-rotated,
+ * FP8-quantised and written to slot pool_idx[v] % 32 of page
+ * block_table[pool_seq[v]][pool_idx[v] / 32].  Fills the cache from a prefill
+ * (one item per pool) and appends the pool a decode step completes (sequences
+ * whose new token makes seq_len % 4 == 0).  An item whose page is outside
+ * [0, n_pages) is skipped and recorded as KPOOL_ERR_INDEX_RANGE. */
+int kpool_paged_append(const void* k, const float* gate, const float* ape, const int32_t* pool_tok,
+                       const int32_t* pool_seq, const int32_t* pool_idx, int32_t n_items,
+                       const int32_t* block_table, int32_t max_pages, int32_t n_pages,
+                       const kpool_params* p, uint8_t* k8_cache, float* sk_cache, int32_t* status,
+                       kpool_stream_t stream);
+
+/* Workspace bytes of dsa_decode_index (0 for an unsupported shape). */
+size_t dsa_decode_workspace_bytes(const kpool_params* p, int32_t B, int32_t max_pages);
+
+/* dsa_decode_index: index rows of one decode step.  The query of sequence b
+ * is its newest token, at position r = seq_lens[b] - 1:
+ *   q_idx bf16 [B, n_idx_heads, d_i], w fp32 [B, n_idx_heads]
+ * It scores the seq_lens[b] / 4 complete pools of its pages, keeps the top
+ * `topk` (higher score, then lower pool), adds its own incomplete pool, and
+ * writes latent-cache slots (page * 128 + offset, i.e. rows of kv_cache seen
+ * as [n_pages * 128, 512]) ascending in position, -1 padded:
+ *   indices int32 [B, W], W a multiple of 4 and >= 4*topk + 3, 16-byte aligned.
+ * The attention of the step is sparse_mla_fwd_rows(q_lat [B, H, 512],
+ * kv_cache, indices, W, n_rows = B, T = n_pages * 128, ...).
+ * workspace: >= dsa_decode_workspace_bytes(p, B, max_pages), 256-byte aligned.
+ * A sequence longer than max_pages * 128 gets an all -1 row and
+ * KPOOL_ERR_SHAPE in *status; a page id outside [0, n_pages) gives
+ * KPOOL_ERR_INDEX_RANGE. */
+int dsa_decode_index(const void* q_idx, const float* w, const uint8_t* k8_cache, const float* sk_cache,
+                     int32_t n_pages, const int32_t* block_table, int32_t max_pages, const int32_t* seq_lens,
+                     int32_t B, int32_t topk, const kpool_params* p, void* workspace, size_t workspace_bytes,
+                     int32_t* indices, int32_t W, int32_t* status, kpool_stream_t stream);
+
 /* kpool_measure_l2_reduce: measurement utility, no counterpart on the pages.
  * Adds 1.0f to each of the 512 floats of rows buf[row_ids[k]], k < n_ids,
  * with fp32 reductions in sparse_mla_bwd's dkv access pattern (each warp

@@ -371,3 +371,33 @@ def sparse_attention_bwd(q_lat, kv_lat, indices, scale, dout, rows, T=None) -> d
         dq[m] = float(scale) * (dz @ kv)
         np.add.at(dkv, valid, p.T @ dout[m] + float(scale) * (dz.T @ q_lat[m]))
     return {"dq": dq, "dkv": dkv, "out": out, "lse": lse}
+
+
+# ----------------------------------------------------------------- 10. paged decode
+
+PAGE_TOKENS = 128
+
+
+def paged_slots(row, block_table_row) -> np.ndarray:
+    """A decode index row in latent-cache slots [PR4036, "Patches and workarounds": 128-token pages of 32
+    pools]: the in-sequence position pos lives in slot block_table_row[pos // 128] * 128 + pos % 128;
+    -1 stays -1."""
+    row = np.asarray(row, dtype=np.int64)
+    bt = np.asarray(block_table_row, dtype=np.int64)
+    out = np.full(row.shape, -1, dtype=np.int64)
+    ok = row >= 0
+    out[ok] = bt[row[ok] // PAGE_TOKENS] * PAGE_TOKENS + row[ok] % PAGE_TOKENS
+    return out
+
+
+def decode_row(q_idx, w, k, gate, ape, topk, W):
+    """Index row of a decode query: the newest token (position L-1) of a sequence of L tokens whose indexer
+    keys and gates are k, gate [L, d_i], with query q_idx [H_i, d_i] and head weights w [H_i].  The same
+    rules as the prefill row of query L-1 of a one-document row (steps 1-7); returns in-sequence positions."""
+    L = np.asarray(k).shape[0]
+    q_all = np.zeros((L,) + np.asarray(q_idx).shape, dtype=np.float32)
+    q_all[L - 1] = np.asarray(q_idx, dtype=np.float32)
+    w_all = np.zeros((L, np.asarray(w).shape[0]), dtype=np.float32)
+    w_all[L - 1] = np.asarray(w, dtype=np.float32)
+    res = indexer(q_all, k, gate, ape, w_all, np.array([0, L]), topk, W, rows=np.array([L - 1]))
+    return res["indices"][0], res

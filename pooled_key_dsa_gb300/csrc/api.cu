@@ -168,6 +168,76 @@ int kpool_measure_l2_reduce(float* buf, int32_t rows, const int32_t* row_ids, in
     return launch_l2_reduce(buf, rows, row_ids, n_ids, reinterpret_cast<cudaStream_t>(stream));
 }
 
+// ---------------------------------------------------------------- paged decode
+
+namespace {
+struct DecodeWs {
+    size_t q8, ws, scores, total;
+};
+DecodeWs decode_ws(int B, int n_idx_heads, int d_idx, int max_pages) {
+    auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+    DecodeWs w;
+    w.q8 = 0;
+    w.ws = up((size_t)B * n_idx_heads * d_idx);
+    w.scores = w.ws + up((size_t)B * n_idx_heads * 4);
+    w.total = w.scores + up((size_t)B * max_pages * 32 * 4);
+    return w;
+}
+bool decode_shape_ok(const kpool_params* p) {
+    return p && p->kpool == KPOOL && p->d_idx == 128 && (p->n_idx_heads == 16 || p->n_idx_heads == 32);
+}
+}  // namespace
+
+size_t dsa_decode_workspace_bytes(const kpool_params* p, int32_t B, int32_t max_pages) {
+    if (!decode_shape_ok(p) || B < 0 || max_pages < 0) return 0;
+    return decode_ws(B, p->n_idx_heads, p->d_idx, max_pages).total;
+}
+
+int kpool_paged_append(const void* k, const float* gate, const float* ape, const int32_t* pool_tok,
+                       const int32_t* pool_seq, const int32_t* pool_idx, int32_t n_items, const int32_t* block_table,
+                       int32_t max_pages, int32_t n_pages, const kpool_params* p, uint8_t* k8_cache, float* sk_cache,
+                       int32_t* status, kpool_stream_t stream) {
+    if (!decode_shape_ok(p)) return p ? KPOOL_ERR_SHAPE : KPOOL_ERR_INVALID_ARG;
+    if (n_items < 0 || max_pages < 1 || n_pages < 1) return KPOOL_ERR_SHAPE;
+    if (n_items == 0) return KPOOL_OK;
+    if (!k || !gate || !ape || !pool_tok || !pool_seq || !pool_idx || !block_table || !k8_cache || !sk_cache)
+        return KPOOL_ERR_INVALID_ARG;
+    if (!aligned(k, 8) || !aligned(gate, 16) || !aligned(ape, 16) || !aligned(k8_cache, 16) || !aligned(sk_cache, 4))
+        return KPOOL_ERR_ALIGN;
+    return launch_paged_append(k, gate, ape, pool_tok, pool_seq, pool_idx, n_items, block_table, max_pages, n_pages,
+                               k8_cache, sk_cache, status, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int dsa_decode_index(const void* q_idx, const float* w, const uint8_t* k8_cache, const float* sk_cache,
+                     int32_t n_pages, const int32_t* block_table, int32_t max_pages, const int32_t* seq_lens,
+                     int32_t B, int32_t topk, const kpool_params* p, void* workspace, size_t workspace_bytes,
+                     int32_t* indices, int32_t W, int32_t* status, kpool_stream_t stream) {
+    if (!p) return KPOOL_ERR_INVALID_ARG;
+    if (!decode_shape_ok(p)) return KPOOL_ERR_SHAPE;
+    if (B < 0 || max_pages < 1 || n_pages < 1 || topk < 1 || W < KPOOL * topk + KPOOL - 1 || (W & 3) != 0)
+        return KPOOL_ERR_SHAPE;
+    if (B == 0) return KPOOL_OK;
+    if (!workspace) return KPOOL_ERR_WORKSPACE;
+    if (!q_idx || !w || !k8_cache || !sk_cache || !block_table || !seq_lens || !indices) return KPOOL_ERR_INVALID_ARG;
+    if (!aligned(q_idx, 8) || !aligned(k8_cache, 16) || !aligned(workspace, 256) || !aligned(indices, 16))
+        return KPOOL_ERR_ALIGN;
+    const DecodeWs o = decode_ws(B, p->n_idx_heads, p->d_idx, max_pages);
+    if (workspace_bytes < o.total) return KPOOL_ERR_WORKSPACE;
+    cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    uint8_t* base = static_cast<uint8_t*>(workspace);
+    uint8_t* q8 = base + o.q8;
+    float* ws = reinterpret_cast<float*>(base + o.ws);
+    float* scores = reinterpret_cast<float*>(base + o.scores);
+    int rc = launch_hadamard_fp8(q_idx, true, (int64_t)B * p->n_idx_heads, p->d_idx, nullptr, w, q8, nullptr, ws, st);
+    if (rc == KPOOL_OK)
+        rc = launch_decode_score(q8, ws, k8_cache, sk_cache, n_pages, block_table, max_pages, seq_lens, B,
+                                 p->n_idx_heads, scores, (int64_t)max_pages * 32, status, st);
+    if (rc == KPOOL_OK)
+        rc = launch_decode_select(scores, (int64_t)max_pages * 32, seq_lens, block_table, max_pages, B, topk, indices,
+                                  W, st);
+    return rc;
+}
+
 int mla_absorb_q(const void* q_nope, const void* w_kv_b, int32_t T, int32_t n_heads, int32_t d_nope, int32_t d_v,
                  void* q_lat, int32_t* status, kpool_stream_t stream) {
     if (T < 0 || !mla_proj_shape_ok(n_heads, d_nope, d_v)) return KPOOL_ERR_SHAPE;
@@ -315,6 +385,6 @@ const char* kpool_strerror(int code) {
 
 // The tags after the arch name identify the kernel generations (used to match
 // stored profiler counters to the code that produced them).
-const char* kpool_version(void) { return "kpooldsa 0.5 sm_103a mla-tc5 score-tc1 select2 proj1 bwd3"; }
+const char* kpool_version(void) { return "kpooldsa 0.6 sm_103a mla-tc5 score-tc1 select2 proj1 bwd3 decode1"; }
 
 }  // extern "C"

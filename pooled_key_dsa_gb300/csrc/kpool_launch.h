@@ -62,6 +62,18 @@ int launch_sparse_mla_bwd(const uint16_t* q_lat, const uint16_t* kv_lat, const i
 // Measurement: fp32 reductions into 512-float rows (the dKv scatter's access pattern).
 int launch_l2_reduce(float* buf, int rows, const int32_t* row_ids, int n_ids, cudaStream_t stream);
 
+// Paged decode (pages of 32 pools = 128 tokens): pooled keys into the page cache; paged FP8 scores
+// scores[b * stride + p] for the complete pools of each sequence; top-k select into cache slots.
+int launch_paged_append(const void* k, const float* gate, const float* ape, const int32_t* pool_tok,
+                        const int32_t* pool_seq, const int32_t* pool_idx, int n_items, const int32_t* block_table,
+                        int max_pages, int n_pages, uint8_t* k8_cache, float* sk_cache, int32_t* status,
+                        cudaStream_t stream);
+int launch_decode_score(const uint8_t* q8, const float* ws, const uint8_t* k8_cache, const float* sk_cache,
+                        int n_pages, const int32_t* block_table, int max_pages, const int32_t* seq_lens, int B,
+                        int n_idx_heads, float* scores, int64_t stride, int32_t* status, cudaStream_t stream);
+int launch_decode_select(const float* scores, int64_t stride, const int32_t* seq_lens, const int32_t* block_table,
+                         int max_pages, int B, int topk, int32_t* indices, int W, cudaStream_t stream);
+
 // Absorbed-MLA projections (absorb: q_nope -> q_lat; otherwise o_lat -> o_v).
 bool mla_proj_shape_ok(int n_heads, int d_nope, int d_v);
 int launch_mla_proj(bool absorb, const void* act, const void* w_kv_b, int T, int n_heads, int d_nope, int d_v,

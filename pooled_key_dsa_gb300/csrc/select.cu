@@ -96,6 +96,20 @@ __device__ void pick_digit(SelectSmem& s, int nbins, uint32_t remaining) {
     __syncthreads();
 }
 
+// Where the positions of a row go: `pool(p)` is the first slot of pool p (the
+// pool's 4 positions are consecutive slots), `tok(pos)` the slot of position
+// pos of the document or sequence.
+struct DocMap {            // packed prefill: slots are global token rows
+    int s_d;
+    __device__ __forceinline__ int pool(int p) const { return s_d + KPOOL * p; }
+    __device__ __forceinline__ int tok(int pos) const { return s_d + pos; }
+};
+struct PageMap {           // paged decode: 128-token pages listed in the sequence's block table
+    const int32_t* bt;
+    __device__ __forceinline__ int pool(int p) const { return bt[p >> 5] * 128 + ((KPOOL * p) & 127); }
+    __device__ __forceinline__ int tok(int pos) const { return bt[pos >> 7] * 128 + (pos & 127); }
+};
+
 constexpr int FAST_KPT = 32;                          // keys per thread on the register path
 constexpr int FAST_MAX = SEL_THREADS * FAST_KPT;     // 8192 candidate pools
 
@@ -136,8 +150,8 @@ __device__ __forceinline__ void column_scan(SelectSmem& s, uint32_t flags, uint3
     __syncthreads();
 }
 
-template <int NC>
-__device__ void select_registers(SelectSmem& s, const float* __restrict__ sc, int n, int topk, int s_d,
+template <int NC, typename Map>
+__device__ void select_registers(SelectSmem& s, const float* __restrict__ sc, int n, int topk, const Map& map,
                                  int32_t* __restrict__ row) {
     const int t = threadIdx.x, wid = t >> 5;
     const uint32_t below = (1u << (t & 31)) - 1u;
@@ -180,7 +194,7 @@ __device__ void select_registers(SelectSmem& s, const float* __restrict__ sc, in
     for (int j = 0; j < NC; ++j) {
         const uint32_t rank = tab[8 * j + wid] + __popc(bal[j] & below);
         if (((take >> j) & 1u) && rank < (uint32_t)topk) {
-            const int pos = s_d + KPOOL * (SEL_THREADS * j + t);
+            const int pos = map.pool(SEL_THREADS * j + t);
             *reinterpret_cast<int4*>(row + KPOOL * rank) = make_int4(pos, pos + 1, pos + 2, pos + 3);
         }
     }
@@ -189,8 +203,10 @@ __device__ void select_registers(SelectSmem& s, const float* __restrict__ sc, in
 }  // namespace
 
 // Streaming path for rows of more than FAST_MAX candidate pools: the row is
-// read from global memory on every pass.
-__device__ void select_streaming(SelectSmem& s, const float* __restrict__ sc, int n, int topk, int s_d, int i,
+// read from global memory on every pass.  r is the query's position in its
+// document or sequence.
+template <typename Map>
+__device__ void select_streaming(SelectSmem& s, const float* __restrict__ sc, int n, int topk, const Map& map, int r,
                                  int tail, int32_t* __restrict__ row, int W) {
     const int t = threadIdx.x;
     // ---- level 1: bits 31..20 over all keys
@@ -261,7 +277,7 @@ __device__ void select_streaming(SelectSmem& s, const float* __restrict__ sc, in
         const int take = gt || (eq && eq_rank < need_eq);
         const int slot = sel_base + block_excl_scan(take, s.warp_tot, sel_tot);
         if (take && slot < topk) {
-            const int pos = s_d + KPOOL * p;
+            const int pos = map.pool(p);
             *reinterpret_cast<int4*>(row + KPOOL * slot) = make_int4(pos, pos + 1, pos + 2, pos + 3);
         }
         sel_base += sel_tot;
@@ -269,7 +285,7 @@ __device__ void select_streaming(SelectSmem& s, const float* __restrict__ sc, in
     }
     for (int j = KPOOL * topk + t; j < W; j += SEL_THREADS) {
         const int q = j - KPOOL * topk;
-        row[j] = q < tail ? i - tail + 1 + q : -1;
+        row[j] = q < tail ? map.tok(r - tail + 1 + q) : -1;
     }
 }
 
@@ -351,28 +367,70 @@ __global__ void __launch_bounds__(SEL_THREADS, 2) select_kernel(const float* __r
         asm volatile("cp.async.commit_group;\n" ::: "memory");
 
         int32_t* row = indices + (int64_t)i * W;
+        const DocMap map{cur.s_d};
         if (cur.d < 0) {
             for (int j = t; j < W; j += SEL_THREADS) row[j] = -1;
         } else if (cur.n <= topk) {                   // every candidate is kept: the causal prefix
-            for (int j = t; j < W; j += SEL_THREADS) row[j] = (j <= cur.r) ? cur.s_d + j : -1;
+            for (int j = t; j < W; j += SEL_THREADS) row[j] = (j <= cur.r) ? map.tok(j) : -1;
         } else if (cur.n <= FAST_MAX) {
             asm volatile("cp.async.wait_group 1;\n" ::: "memory");
             __syncthreads();
             const float* sc = rowbuf + (k & 1) * ROWBUF + (int)(cur.start & 3);
-            if (cur.n <= 8 * SEL_THREADS) select_registers<8>(s, sc, cur.n, topk, cur.s_d, row);
-            else if (cur.n <= 16 * SEL_THREADS) select_registers<16>(s, sc, cur.n, topk, cur.s_d, row);
-            else select_registers<32>(s, sc, cur.n, topk, cur.s_d, row);
+            if (cur.n <= 8 * SEL_THREADS) select_registers<8>(s, sc, cur.n, topk, map, row);
+            else if (cur.n <= 16 * SEL_THREADS) select_registers<16>(s, sc, cur.n, topk, map, row);
+            else select_registers<32>(s, sc, cur.n, topk, map, row);
             for (int j = KPOOL * topk + t; j < W; j += SEL_THREADS) {
                 const int q = j - KPOOL * topk;
-                row[j] = q < cur.tail ? i - cur.tail + 1 + q : -1;
+                row[j] = q < cur.tail ? map.tok(cur.r - cur.tail + 1 + q) : -1;
             }
         } else {
-            select_streaming(s, scores + cur.start, cur.n, topk, cur.s_d, i, cur.tail, row, W);
+            select_streaming(s, scores + cur.start, cur.n, topk, map, cur.r, cur.tail, row, W);
         }
         __syncthreads();                              // the row buffer and s are reused
         cur = nxt;
     }
     asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+}
+
+// Paged decode: one block per sequence b, whose query is its last token
+// (position r = seq_lens[b] - 1).  Its n = seq_lens[b] / 4 complete pools have
+// scores at scores[b * stride + p]; positions map to latent-cache slots through
+// the sequence's row of the block table.
+__global__ void __launch_bounds__(SEL_THREADS) decode_select_kernel(const float* __restrict__ scores, int64_t stride,
+                                                                    const int32_t* __restrict__ seq_lens,
+                                                                    const int32_t* __restrict__ block_table,
+                                                                    int max_pages, int topk,
+                                                                    int32_t* __restrict__ indices, int W) {
+    __shared__ SelectSmem s;
+    const int t = threadIdx.x, b = blockIdx.x;
+    const int L = seq_lens[b];
+    int32_t* row = indices + (int64_t)b * W;
+    const PageMap map{block_table + (int64_t)b * max_pages};
+    const int r = L - 1, n = L / KPOOL, tail = L % KPOOL;
+    const float* sc = scores + (int64_t)b * stride;
+    if (L <= 0 || L > max_pages * 128) {              // empty, or more than the block table holds
+        for (int j = t; j < W; j += SEL_THREADS) row[j] = -1;
+    } else if (n <= topk) {
+        for (int j = t; j < W; j += SEL_THREADS) row[j] = (j <= r) ? map.tok(j) : -1;
+    } else if (n <= FAST_MAX) {
+        if (n <= 8 * SEL_THREADS) select_registers<8>(s, sc, n, topk, map, row);
+        else if (n <= 16 * SEL_THREADS) select_registers<16>(s, sc, n, topk, map, row);
+        else select_registers<32>(s, sc, n, topk, map, row);
+        for (int j = KPOOL * topk + t; j < W; j += SEL_THREADS) {
+            const int q = j - KPOOL * topk;
+            row[j] = q < tail ? map.tok(r - tail + 1 + q) : -1;
+        }
+    } else {
+        select_streaming(s, sc, n, topk, map, r, tail, row, W);
+    }
+}
+
+int launch_decode_select(const float* scores, int64_t stride, const int32_t* seq_lens, const int32_t* block_table,
+                         int max_pages, int B, int topk, int32_t* indices, int W, cudaStream_t stream) {
+    if (B <= 0) return KPOOL_OK;
+    decode_select_kernel<<<B, SEL_THREADS, 0, stream>>>(scores, stride, seq_lens, block_table, max_pages, topk,
+                                                        indices, W);
+    return cudaGetLastError() == cudaSuccess ? KPOOL_OK : KPOOL_ERR_CUDA;
 }
 
 int launch_select(const float* scores, const int64_t* pair_base, const kpool_layout& L, int topk, int32_t* indices,

@@ -23,7 +23,8 @@ CODES = {v: k for k, v in ERRORS.items()}
 EXPORTED = ("kpool_workspace_bytes", "kpool_workspace_offsets", "kpool_build", "dsa_index", "sparse_mla_fwd",
             "kpool_stage_select", "kpool_set_stage_events", "kpool_check_status", "kpool_strerror", "kpool_version",
             "dsa_index_noalloc", "sparse_mla_fwd_rows", "kpool_forward_host", "mla_absorb_q", "mla_v_proj",
-            "sparse_mla_bwd", "kpool_measure_l2_reduce")
+            "sparse_mla_bwd", "kpool_measure_l2_reduce", "kpool_paged_append", "dsa_decode_workspace_bytes",
+            "dsa_decode_index")
 
 
 class KpoolUnavailable(ImportError):
@@ -90,6 +91,12 @@ def lib():
                                          ctypes.POINTER(Params), i32, vp, vp, vp]
         L.sparse_mla_bwd.argtypes = [vp, vp, vp, i32, i32, i32, ctypes.c_float, vp, vp, vp, vp, vp, vp, vp, vp]
         L.kpool_measure_l2_reduce.argtypes = [vp, i32, vp, i32, vp]
+        L.kpool_paged_append.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, ctypes.POINTER(Params), vp, vp,
+                                         vp, vp]
+        L.dsa_decode_workspace_bytes.argtypes = [ctypes.POINTER(Params), i32, i32]
+        L.dsa_decode_workspace_bytes.restype = sz
+        L.dsa_decode_index.argtypes = [vp, vp, vp, vp, i32, vp, i32, vp, i32, i32, ctypes.POINTER(Params), vp, sz, vp,
+                                       i32, vp, vp]
         L.mla_absorb_q.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp]
         L.mla_v_proj.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp]
         L.kpool_stage_select.argtypes = [vp, vp, ctypes.POINTER(LayoutC), i32, vp, i32, vp]
@@ -307,6 +314,52 @@ def measure_l2_reduce(buf, row_ids, stream=None):
         raise ValueError("buf must be [rows, 512]")
     _check(lib().kpool_measure_l2_reduce(_ptr(buf), buf.shape[0], _ptr(row_ids), row_ids.numel(), _stream(stream)),
            "kpool_measure_l2_reduce")
+
+
+# ----------------------------------------------------------------- paged decode
+
+PAGE_TOKENS = 128          # tokens per page (32 pools of 4)
+
+
+def decode_workspace_bytes(p: Params, B: int, max_pages: int) -> int:
+    return int(lib().dsa_decode_workspace_bytes(ctypes.byref(p), B, max_pages))
+
+
+def paged_append(k, gate, ape, pool_tok, pool_seq, pool_idx, block_table, n_pages: int, p: Params, k8_cache, sk_cache,
+                 status=None, stream=None):
+    """Pooled keys of the 4-token rows pool_tok[v].. of k/gate into slot pool_idx[v] of sequence pool_seq[v]'s
+    pages (block_table [B, max_pages]) of the caches k8_cache uint8 [n_pages, 32, d_i], sk_cache fp32 [n_pages, 32]."""
+    n = pool_tok.numel()
+    for name, t in (("pool_tok", pool_tok), ("pool_seq", pool_seq), ("pool_idx", pool_idx)):
+        _want(t, torch.int32, (n,), name)
+    _want(block_table, torch.int32, None, "block_table")
+    _want(k8_cache, torch.uint8, (n_pages, 32, p.d_idx), "k8_cache")
+    _want(sk_cache, torch.float32, (n_pages, 32), "sk_cache")
+    _check(lib().kpool_paged_append(_ptr(k), _ptr(gate), _ptr(ape), _ptr(pool_tok), _ptr(pool_seq), _ptr(pool_idx), n,
+                                    _ptr(block_table), block_table.shape[1], n_pages, ctypes.byref(p), _ptr(k8_cache),
+                                    _ptr(sk_cache), _ptr(status), _stream(stream)), "kpool_paged_append")
+
+
+def decode_index(q_idx, w, k8_cache, sk_cache, block_table, seq_lens, topk: int, p: Params, W: int,
+                 workspace=None, indices=None, status=None, stream=None):
+    """Index rows of one decode step: latent-cache slots [B, W] for each sequence's newest token."""
+    B = q_idx.shape[0]
+    n_pages = k8_cache.shape[0]
+    _want(q_idx, torch.bfloat16, (B, p.n_idx_heads, p.d_idx), "q_idx")
+    _want(w, torch.float32, (B, p.n_idx_heads), "w")
+    _want(block_table, torch.int32, None, "block_table")
+    _want(seq_lens, torch.int32, (B,), "seq_lens")
+    max_pages = block_table.shape[1]
+    need = decode_workspace_bytes(p, B, max_pages)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q_idx.device)
+    if indices is None:
+        indices = torch.empty((B, W), dtype=torch.int32, device=q_idx.device)
+    _check(lib().dsa_decode_index(_ptr(q_idx), _ptr(w), _ptr(k8_cache), _ptr(sk_cache), n_pages, _ptr(block_table),
+                                  max_pages, _ptr(seq_lens), B, topk, ctypes.byref(p), _ptr(workspace),
+                                  workspace.numel(), _ptr(indices), W, _ptr(status), _stream(stream)),
+           "dsa_decode_index")
+    return indices
 
 
 def _proj_weight(w_kv_b, H: int, d_nope: int, d_v: int, D: int):

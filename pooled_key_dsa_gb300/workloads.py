@@ -221,3 +221,99 @@ def all_inputs(wl: Workload) -> Inputs:
     inp = indexer_inputs(wl)
     inp.q_lat = q_lat(wl)
     return inp
+
+
+# --------------------------------------------------------------------------- paged decode
+
+_DEC_LENS, _DEC_PAGES, _DEC_K, _DEC_GATE, _DEC_APE, _DEC_KV, _DEC_QIDX, _DEC_W, _DEC_QLAT = range(32, 41)
+PAGE_TOKENS = 128          # 32 pools of 4 per page (vLLM's index_kpool x 32 block)
+
+
+@dataclass(frozen=True)
+class DecodeWorkload:
+    """One decode step over B sequences: sequence b holds seq_lens[b] tokens, the last of which is the
+    step's query.  Each sequence is one document; its latent rows and pooled keys live in 128-token pages
+    assigned by a seeded permutation (so the block table is not the identity)."""
+    name: str
+    seed: int
+    seq_lens: tuple
+    n_idx_heads: int = 32
+    d_idx: int = 128
+    topk: int = 512
+    n_heads: int = 64
+    d_lat: int = 512
+    kpool: int = 4
+    spare_pages: int = 3
+
+    @property
+    def B(self) -> int:
+        return len(self.seq_lens)
+
+    @property
+    def W(self) -> int:
+        raw = self.kpool * self.topk + self.kpool - 1
+        return 128 * ((raw + 127) // 128)
+
+    @property
+    def pages_per_seq(self) -> list:
+        return [(L + PAGE_TOKENS - 1) // PAGE_TOKENS for L in self.seq_lens]
+
+    @property
+    def max_pages(self) -> int:
+        return max(max(self.pages_per_seq), 1)
+
+    @property
+    def n_pages(self) -> int:
+        return sum(self.pages_per_seq) + self.spare_pages
+
+    @property
+    def scale(self) -> float:
+        return float(np.float32(1.0 / math.sqrt(self.d_lat)))
+
+    def block_table(self) -> np.ndarray:
+        """int32 [B, max_pages]: a seeded permutation of the pages, -1 past each sequence's last page."""
+        perm = np.random.default_rng([self.seed, _DEC_PAGES]).permutation(self.n_pages).astype(np.int32)
+        bt = np.full((self.B, self.max_pages), -1, np.int32)
+        at = 0
+        for b, npg in enumerate(self.pages_per_seq):
+            bt[b, :npg] = perm[at:at + npg]
+            at += npg
+        return bt
+
+
+def decode_workload(idx: int) -> DecodeWorkload:
+    if idx == 0:      # tiny: every branch of a row (all pools kept, radix select, tails 0..3, several pages)
+        return DecodeWorkload("decode_tiny", 50, (5, 9, 130, 517, 1029, 1100, 2052, 2175), topk=64)
+    if idx == 1:      # rows of > 8192 pools take the streaming select
+        return DecodeWorkload("decode_long_rows", 51, (33000, 40003, 4099))
+    if idx == 2:      # benchmark: 128 sequences, lengths log-uniform in [4096, 32768]
+        rng = np.random.default_rng([52, _DEC_LENS])
+        lens = np.exp(rng.uniform(math.log(4096), math.log(32768), size=128)).astype(np.int64)
+        return DecodeWorkload("decode_B128_loguniform_4K_32K", 52, tuple(int(x) for x in lens))
+    raise ValueError(f"no decode workload {idx}")
+
+
+@dataclass
+class DecodeInputs:
+    dw: DecodeWorkload
+    k: list            # per sequence, bf16 [L_b, d_i]
+    gate: list         # per sequence, fp32 [L_b, d_i]
+    kv_lat: list       # per sequence, bf16 [L_b, D]
+    ape: np.ndarray    # fp32 [kpool, d_i]
+    q_idx: torch.Tensor  # bf16 [B, H_i, d_i], the newest token of each sequence
+    w: np.ndarray      # fp32 [B, H_i]
+    q_lat: torch.Tensor  # bf16 [B, H, D]
+
+
+def decode_inputs(dw: DecodeWorkload) -> DecodeInputs:
+    """Host inputs of a decode workload (small and medium sizes; the benchmark draws its caches on the GPU)."""
+    ks, gs, kvs = [], [], []
+    for b, L in enumerate(dw.seq_lens):
+        ks.append(_bf16(_normal(dw.seed, _DEC_K, (L, dw.d_idx), chunk=b)))
+        gs.append(_normal(dw.seed, _DEC_GATE, (L, dw.d_idx), chunk=b))
+        kvs.append(_bf16(_normal(dw.seed, _DEC_KV, (L, dw.d_lat), chunk=b)))
+    ape = _normal(dw.seed, _DEC_APE, (dw.kpool, dw.d_idx), std=0.1)
+    q_idx = _bf16(_normal(dw.seed, _DEC_QIDX, (dw.B, dw.n_idx_heads, dw.d_idx)))
+    w = (_normal(dw.seed, _DEC_W, (dw.B, dw.n_idx_heads)) / np.float32(math.sqrt(dw.n_idx_heads))).astype(np.float32)
+    q_lat = _bf16(_normal(dw.seed, _DEC_QLAT, (dw.B, dw.n_heads, dw.d_lat)))
+    return DecodeInputs(dw, ks, gs, kvs, ape, q_idx, w, q_lat)

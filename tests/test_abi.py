@@ -150,6 +150,36 @@ def test_host_checks_of_the_backward_entry(lib):
     assert red(None, 8, None, 0, None) == K.KPOOL_OK
 
 
+def test_host_checks_of_the_decode_entries(lib):
+    vp = ctypes.c_void_p
+    p = K.make_params()
+    bad = K.make_params(d_idx=64, n_idx_heads=4)
+    assert lib.dsa_decode_workspace_bytes(ctypes.byref(bad), 4, 8) == 0
+    assert lib.dsa_decode_workspace_bytes(ctypes.byref(p), 4, 8) >= 4 * 8 * 32 * 4
+    ok = [vp(16)] * 4
+    # unsupported shape, W too small or not a multiple of 4, workspace too small, B = 0 is a no-op
+    assert lib.dsa_decode_index(*ok, 8, vp(16), 8, vp(16), 4, 512, ctypes.byref(bad), vp(256), 1 << 20, vp(16), 2176,
+                                None, None) == K.CODES["KPOOL_ERR_SHAPE"]
+    assert lib.dsa_decode_index(*ok, 8, vp(16), 8, vp(16), 4, 512, ctypes.byref(p), vp(256), 1 << 20, vp(16), 2050,
+                                None, None) == K.CODES["KPOOL_ERR_SHAPE"]
+    assert lib.dsa_decode_index(*ok, 8, vp(16), 8, vp(16), 4, 512, ctypes.byref(p), vp(256), 1 << 20, vp(16), 2178,
+                                None, None) == K.CODES["KPOOL_ERR_SHAPE"]
+    assert lib.dsa_decode_index(*ok, 8, vp(16), 8, vp(16), 4, 512, ctypes.byref(p), vp(256), 16, vp(16), 2176,
+                                None, None) == K.CODES["KPOOL_ERR_WORKSPACE"]
+    assert lib.dsa_decode_index(*ok, 8, vp(16), 8, vp(16), 4, 512, ctypes.byref(p), vp(256), 1 << 20, vp(8), 2176,
+                                None, None) == K.CODES["KPOOL_ERR_ALIGN"]
+    assert lib.dsa_decode_index(None, None, None, None, 8, None, 8, None, 0, 512, ctypes.byref(p), None, 0, None,
+                                2176, None, None) == K.KPOOL_OK
+    app = lib.kpool_paged_append
+    assert app(*([vp(16)] * 6), 4, vp(16), 8, 8, ctypes.byref(bad), vp(16), vp(16), None, None) == \
+        K.CODES["KPOOL_ERR_SHAPE"]
+    assert app(*([vp(16)] * 6), 4, vp(16), 0, 8, ctypes.byref(p), vp(16), vp(16), None, None) == \
+        K.CODES["KPOOL_ERR_SHAPE"]
+    assert app(vp(16), vp(16), vp(16), None, vp(16), vp(16), 4, vp(16), 8, 8, ctypes.byref(p), vp(16), vp(16), None,
+               None) == K.CODES["KPOOL_ERR_INVALID_ARG"]
+    assert app(*([None] * 6), 0, None, 8, 8, ctypes.byref(p), None, None, None, None) == K.KPOOL_OK
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(K, "_lib", None)
     monkeypatch.setattr(K, "_LIB_PATH", str(tmp_path / "missing.so"))

@@ -389,3 +389,23 @@ def test_attention_empty_row():
     out, lse = O.sparse_attention(np.ones((1, 2, 4), np.float32), np.ones((3, 4), np.float32),
                                   np.full((1, 128), -1, np.int32), 1.0, [0])
     assert not out.any() and np.all(np.isneginf(lse))
+
+
+# ----------------------------------------------------------------- paged decode
+
+def test_paged_slots_hand_example():
+    bt = [7, 2, 5]                       # pages of positions 0-127, 128-255, 256-383
+    row = [0, 1, 127, 128, 255, 256, 300, -1]
+    assert O.paged_slots(row, bt).tolist() == [896, 897, 1023, 256, 383, 640, 684, -1]
+
+
+def test_decode_row_is_the_prefill_row_of_the_last_token():
+    wl = workloads.workload(1)                 # one document: the decode query is its last token
+    inp = workloads.indexer_inputs(wl)
+    L = 700
+    k = inp.k[:L].float().numpy()
+    row, _ = O.decode_row(inp.q_idx[L - 1].float().numpy(), inp.w[L - 1], k, inp.gate[:L], inp.ape, 64,
+                          O.row_width(64))
+    full = O.indexer(inp.q_idx[:L].float().numpy(), k, inp.gate[:L], inp.ape, inp.w[:L], np.array([0, L]), 64,
+                     O.row_width(64), rows=np.array([L - 1]))
+    assert np.array_equal(row, full["indices"][0])
