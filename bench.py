@@ -51,6 +51,8 @@ def _args():
                     help="profiling aid: run the absorbed-MLA projections only (mla_absorb_q, mla_v_proj)")
     ap.add_argument("--only-bwd", action="store_true",
                     help="profiling aid: index rows and the forward once, then time sparse_mla_bwd only")
+    ap.add_argument("--only-decode", action="store_true",
+                    help="profiling aid: run the paged decode step only")
     ap.add_argument("--d-nope", type=int, default=128, help="per-head key width of the absorbed projection")
     ap.add_argument("--d-v", type=int, default=128, help="per-head value width of the V projection")
     return ap.parse_args()
@@ -360,6 +362,80 @@ def run_bwd(a, wl, K, dev, q, kv, idx, out, lse, valid_slots, flush):
             "what": "sparse_mla_bwd (delta, dQ, dKV) on the step's index rows and forward results, seeded dout"}
 
 
+def run_decode(a, K, dev, flush=None, cfg=2):
+    """One paged decode step over B sequences (the newest token of each is the query): the pool it completes
+    appended to the page cache (sequences with seq_len % 4 == 0), dsa_decode_index (Hadamard/FP8 of the B
+    queries, paged FP8 scoring, select into latent-cache slots) and the sparse attention over the paged latent
+    cache.  The caches hold every earlier token; they are drawn on the GPU from a seeded generator."""
+    import torch
+    from pooled_key_dsa_gb300 import workloads
+    dw = workloads.decode_workload(cfg)
+    B, lens, d_i, D = dw.B, np.asarray(dw.seq_lens, np.int64), dw.d_idx, dw.d_lat
+    bt_h = dw.block_table()
+    starts = np.concatenate([[0], np.cumsum(lens)])[:-1]
+    total = int(lens.sum())
+    g = torch.Generator(device=dev).manual_seed(dw.seed)
+    k = torch.randn((total, d_i), generator=g, device=dev).to(torch.bfloat16)
+    gate = torch.randn((total, d_i), generator=g, device=dev)
+    ape = torch.randn((4, d_i), generator=g, device=dev) * 0.1
+    p = K.make_params(topk=dw.topk, n_idx_heads=dw.n_idx_heads, d_idx=d_i, n_heads=dw.n_heads, d_lat=D,
+                      scale=dw.scale)
+    bt = torch.from_numpy(bt_h).to(dev)
+    k8 = torch.zeros((dw.n_pages, 32, d_i), dtype=torch.uint8, device=dev)
+    sk = torch.zeros((dw.n_pages, 32), dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    # every pool except the one this step completes (untimed cache fill)
+    done = lens // 4 - (lens % 4 == 0)
+    seq = np.repeat(np.arange(B), done).astype(np.int32)
+    idx = np.concatenate([np.arange(n) for n in done]).astype(np.int32)
+    tok = (starts[seq] + 4 * idx).astype(np.int32)
+    t32 = lambda x: torch.from_numpy(np.ascontiguousarray(x, dtype=np.int32)).to(dev)
+    K.paged_append(k, gate, ape, t32(tok), t32(seq), t32(idx), bt, dw.n_pages, p, k8, sk, status=status)
+    # the pools the step completes
+    comp = np.nonzero(lens % 4 == 0)[0]
+    a_tok, a_seq, a_idx = t32(starts[comp] + lens[comp] - 4), t32(comp), t32(lens[comp] // 4 - 1)
+    kv = torch.randn((dw.n_pages * workloads.PAGE_TOKENS, D), generator=g, device=dev).to(torch.bfloat16)
+    q_idx = torch.randn((B, dw.n_idx_heads, d_i), generator=g, device=dev).to(torch.bfloat16)
+    w = torch.randn((B, dw.n_idx_heads), generator=g, device=dev) / math.sqrt(dw.n_idx_heads)
+    q_lat = torch.randn((B, dw.n_heads, D), generator=g, device=dev).to(torch.bfloat16)
+    seq_lens = t32(lens)
+    wsb = torch.empty(K.decode_workspace_bytes(p, B, dw.max_pages), dtype=torch.uint8, device=dev)
+    rows = torch.empty((B, dw.W), dtype=torch.int32, device=dev)
+    out = torch.empty_like(q_lat)
+    lse = torch.empty((B, dw.n_heads), dtype=torch.float32, device=dev)
+    if flush is None:
+        flush = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+    ev = []
+    for s in range(a.warmup + a.steps):
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        flush.zero_()
+        e[0].record(stream)
+        if len(comp):
+            K.paged_append(k, gate, ape, a_tok, a_seq, a_idx, bt, dw.n_pages, p, k8, sk, status=status)
+        e[1].record(stream)
+        K.decode_index(q_idx, w, k8, sk, bt, seq_lens, dw.topk, p, dw.W, workspace=wsb, indices=rows, status=status)
+        e[2].record(stream)
+        K.sparse_mla_fwd_rows(q_lat, kv, rows, dw.scale, out=out, lse=lse, status=status)
+        e[3].record(stream)
+        if s >= a.warmup:
+            ev.append(e)
+    torch.cuda.synchronize()
+    st = K.check_status(status)
+    ms = lambda i, j: statistics.mean(x[i].elapsed_time(x[j]) for x in ev)
+    step, app, idx_ms, att = ms(0, 3), ms(0, 1), ms(1, 2), ms(2, 3)
+    valid = int((rows >= 0).sum().item())
+    res = {"workload": f"{dw.name}: {B} sequences, {total} cached tokens, {dw.n_pages} pages of 128 tokens",
+           "status": st, "ms_per_step": step, "tokens_per_s": B / (step / 1e3),
+           "stage_ms": {"append": app, "decode_index": idx_ms, "sparse_mla": att},
+           "pools_appended": int(len(comp)), "valid_slots": valid,
+           "attention_gather_GBs": valid * D * 2 / att / 1e6,
+           "attention_TFLOPs": 2.0 * dw.n_heads * 2 * D * valid / att / 1e9,
+           "what": "one decode step: pool append, paged indexer, sparse attention over the paged latent cache"}
+    del k, gate, kv, k8, sk, q_idx, q_lat, out, wsb, rows
+    return res
+
+
 # ----------------------------------------------------------------- our arm
 
 def main():
@@ -386,6 +462,9 @@ def main():
     K.lib()
 
     wl = workloads.workload(a.config)
+    if a.only_decode:
+        print(json.dumps({"mode": "decode_only", "decode": run_decode(a, K, torch.device("cuda", local))}))
+        return
     if a.only_proj:
         print(json.dumps({"mode": "proj_only", "config": _config(wl), "absorb": run_proj(a, wl, K,
                                                                                          torch.device("cuda", local))}))
@@ -522,6 +601,8 @@ def main():
     proj = run_proj(a, wl, K, dev, o_lat=out, flush=flush)
     # ---- the backward of the attention on this step's rows and results
     bwd = run_bwd(a, wl, K, dev, d["q_lat"], d["kv_lat"], idx, out, lse, _work(wl)["valid_slots"], flush)
+    # ---- a paged decode step (its own workload)
+    dec = run_decode(a, K, dev, flush)
     e2e_ms = sum(x.elapsed_time(y) for x, y in e2e_ev)
     tm = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
     if world > 1:
@@ -567,6 +648,7 @@ def main():
                              "what": "a shared DSA layer: sparse_mla_fwd only, on the index rows of the step"},
         "absorb": proj,
         "sparse_mla_bwd": bwd,
+        "decode": dec,
         "wall_s_timed": wall,
     }
     if world == 1 and not a.no_cpu_baseline:

@@ -28,105 +28,99 @@ constexpr int PAGE_POOLS = 32;
 constexpr int PAGE_TOKENS = PAGE_POOLS * KPOOL;   // 128
 
 // ---------------------------------------------------------------- paged append
-// One warp per pooled key: lane l pools channels 4l .. 4l+3 of the 4 token rows
-// starting at row pool_tok[v] of k / gate (fp64 softmax(gate + ape) weights,
-// rounded once to fp32), then the same butterfly, scale and E4M3 cast as the
-// prefill's key quantisation (lane l holds elements 4l .. 4l+3 of the vector),
-// and writes codes and scale to slot pool_idx[v] % 32 of page
+// One 128-thread block per pooled key.  Thread c pools channel c of the 4 token
+// rows starting at row pool_tok[v] of k / gate (fp64 softmax(gate + ape)
+// weights, rounded once to fp32: the prefill pooling's arithmetic, spread over
+// 128 threads because fp64 is slow on this part).  Warp 0 then applies the
+// prefill's key quantisation (lane l holds elements 4l .. 4l+3: butterfly,
+// scale, E4M3 cast) and writes codes and scale to slot pool_idx[v] % 32 of page
 // block_table[pool_seq[v]][pool_idx[v] / 32].  d_i = 128.
-__global__ void __launch_bounds__(256) paged_append_kernel(
+__global__ void __launch_bounds__(128) paged_append_kernel(
     const uint16_t* __restrict__ k, const float* __restrict__ gate, const float* __restrict__ ape,
     const int32_t* __restrict__ pool_tok, const int32_t* __restrict__ pool_seq, const int32_t* __restrict__ pool_idx,
     int n_items, const int32_t* __restrict__ block_table, int max_pages, int n_pages, uint8_t* __restrict__ k8_cache,
     float* __restrict__ sk_cache, int32_t* status) {
     constexpr int D = 128, E = 4;
-    const int lane = threadIdx.x & 31;
-    const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    __shared__ __align__(16) float pooled[D];
+    const int tid = threadIdx.x, lane = tid & 31;
     const float c = 0.08838834764831845f;          // fp32(1/sqrt(128))
-    for (int64_t v = warp0; v < n_items; v += nwarps) {
+    for (int64_t v = blockIdx.x; v < n_items; v += gridDim.x) {
         const int pidx = pool_idx[v];
         const int pj = pidx / PAGE_POOLS;
         const int page = (pidx >= 0 && pj < max_pages) ? block_table[(int64_t)pool_seq[v] * max_pages + pj] : -1;
-        if (page < 0 || page >= n_pages) {
-            if (lane == 0) set_status(status, KPOOL_ERR_INDEX_RANGE);
+        if (page < 0 || page >= n_pages) {         // uniform over the block
+            if (tid == 0) set_status(status, KPOOL_ERR_INDEX_RANGE);
             continue;
         }
         const int64_t t0 = pool_tok[v];
-        const int ch = lane * E;
-        double lg[KPOOL][E], kv[KPOOL][E];
+        {
+            double lg[KPOOL], kv[KPOOL];
 #pragma unroll
-        for (int j = 0; j < KPOOL; ++j) {
-            const float4 g = *reinterpret_cast<const float4*>(gate + (t0 + j) * D + ch);
-            const float4 a = *reinterpret_cast<const float4*>(ape + j * D + ch);
-            const uint2 kb = *reinterpret_cast<const uint2*>(k + (t0 + j) * D + ch);
-            lg[j][0] = __dadd_rn((double)g.x, (double)a.x);
-            lg[j][1] = __dadd_rn((double)g.y, (double)a.y);
-            lg[j][2] = __dadd_rn((double)g.z, (double)a.z);
-            lg[j][3] = __dadd_rn((double)g.w, (double)a.w);
-            kv[j][0] = (double)bf16_bits_to_float((uint16_t)(kb.x & 0xffffu));
-            kv[j][1] = (double)bf16_bits_to_float((uint16_t)(kb.x >> 16));
-            kv[j][2] = (double)bf16_bits_to_float((uint16_t)(kb.y & 0xffffu));
-            kv[j][3] = (double)bf16_bits_to_float((uint16_t)(kb.y >> 16));
-        }
-        float e[E];
+            for (int j = 0; j < KPOOL; ++j) {
+                lg[j] = __dadd_rn((double)gate[(t0 + j) * D + tid], (double)ape[j * D + tid]);
+                kv[j] = (double)bf16_bits_to_float(k[(t0 + j) * D + tid]);
+            }
+            double m = lg[0];
 #pragma unroll
-        for (int q = 0; q < E; ++q) {
-            double m = lg[0][q];
-#pragma unroll
-            for (int j = 1; j < KPOOL; ++j) m = fmax(m, lg[j][q]);
+            for (int j = 1; j < KPOOL; ++j) m = fmax(m, lg[j]);
             double w[KPOOL], s = 0.0;
 #pragma unroll
             for (int j = 0; j < KPOOL; ++j) {
-                w[j] = exp(__dsub_rn(lg[j][q], m));
+                w[j] = exp(__dsub_rn(lg[j], m));
                 s = __dadd_rn(s, w[j]);
             }
             double acc = 0.0;
 #pragma unroll
-            for (int j = 0; j < KPOOL; ++j) acc = __dadd_rn(acc, __dmul_rn(__ddiv_rn(w[j], s), kv[j][q]));
-            e[q] = (float)acc;
+            for (int j = 0; j < KPOOL; ++j) acc = __dadd_rn(acc, __dmul_rn(__ddiv_rn(w[j], s), kv[j]));
+            pooled[tid] = (float)acc;
         }
-        // butterfly: strides 1, 2 inside the thread, then 4 .. 64 across lanes
+        __syncthreads();
+        if (tid < 32) {
+            const float4 x = *reinterpret_cast<const float4*>(pooled + lane * E);
+            float e[E] = {x.x, x.y, x.z, x.w};
+            // butterfly: strides 1, 2 inside the thread, then 4 .. 64 across lanes
 #pragma unroll
-        for (int h = 1; h < E; h <<= 1)
+            for (int h = 1; h < E; h <<= 1)
 #pragma unroll
-            for (int j = 0; j < E; ++j)
-                if ((j & h) == 0) {
-                    const float a = e[j], b = e[j + h];
-                    e[j] = __fadd_rn(a, b);
-                    e[j + h] = __fsub_rn(a, b);
+                for (int j = 0; j < E; ++j)
+                    if ((j & h) == 0) {
+                        const float a = e[j], b = e[j + h];
+                        e[j] = __fadd_rn(a, b);
+                        e[j + h] = __fsub_rn(a, b);
+                    }
+#pragma unroll
+            for (int lb = 1; lb < 32; lb <<= 1) {
+                const bool high = (lane & lb) != 0;
+#pragma unroll
+                for (int j = 0; j < E; ++j) {
+                    const float other = __shfl_xor_sync(0xffffffffu, e[j], lb);
+                    e[j] = high ? __fsub_rn(other, e[j]) : __fadd_rn(e[j], other);
                 }
-#pragma unroll
-        for (int lb = 1; lb < 32; lb <<= 1) {
-            const bool high = (lane & lb) != 0;
+            }
+            float amax = 0.f;
 #pragma unroll
             for (int j = 0; j < E; ++j) {
-                const float other = __shfl_xor_sync(0xffffffffu, e[j], lb);
-                e[j] = high ? __fsub_rn(other, e[j]) : __fadd_rn(e[j], other);
+                e[j] = __fmul_rn(e[j], c);
+                amax = fmaxf(amax, fabsf(e[j]));
             }
-        }
-        float amax = 0.f;
 #pragma unroll
-        for (int j = 0; j < E; ++j) {
-            e[j] = __fmul_rn(e[j], c);
-            amax = fmaxf(amax, fabsf(e[j]));
+            for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+            uint32_t packed = 0;
+            float sc = 0.f;
+            if (amax > 0.f) {
+                const float inv = __fdiv_rn(448.f, amax);
+                sc = __fdiv_rn(amax, 448.f);
+                const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
+                    make_float2(__fmul_rn(e[0], inv), __fmul_rn(e[1], inv)), __NV_SATFINITE, __NV_E4M3);
+                const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
+                    make_float2(__fmul_rn(e[2], inv), __fmul_rn(e[3], inv)), __NV_SATFINITE, __NV_E4M3);
+                packed = (uint32_t)lo | ((uint32_t)hi << 16);
+            }
+            const int64_t slot = (int64_t)page * PAGE_POOLS + (pidx % PAGE_POOLS);
+            *reinterpret_cast<uint32_t*>(k8_cache + slot * D + lane * E) = packed;
+            if (lane == 0) sk_cache[slot] = sc;
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        uint32_t packed = 0;
-        float sc = 0.f;
-        if (amax > 0.f) {
-            const float inv = __fdiv_rn(448.f, amax);
-            sc = __fdiv_rn(amax, 448.f);
-            const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
-                make_float2(__fmul_rn(e[0], inv), __fmul_rn(e[1], inv)), __NV_SATFINITE, __NV_E4M3);
-            const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
-                make_float2(__fmul_rn(e[2], inv), __fmul_rn(e[3], inv)), __NV_SATFINITE, __NV_E4M3);
-            packed = (uint32_t)lo | ((uint32_t)hi << 16);
-        }
-        const int64_t slot = (int64_t)page * PAGE_POOLS + (pidx % PAGE_POOLS);
-        *reinterpret_cast<uint32_t*>(k8_cache + slot * D + ch) = packed;
-        if (lane == 0) sk_cache[slot] = sc;
+        __syncthreads();                             // `pooled` is rewritten for the next item
     }
 }
 
@@ -267,8 +261,8 @@ int launch_paged_append(const void* k, const float* gate, const float* ape, cons
                         int max_pages, int n_pages, uint8_t* k8_cache, float* sk_cache, int32_t* status,
                         cudaStream_t stream) {
     if (n_items <= 0) return KPOOL_OK;
-    const int64_t blocks = ((int64_t)n_items + 7) / 8;
-    paged_append_kernel<<<(unsigned)(blocks < 152 * 64 ? blocks : 152 * 64), 256, 0, stream>>>(
+    const int64_t blocks = n_items < 152 * 64 ? n_items : 152 * 64;
+    paged_append_kernel<<<(unsigned)blocks, 128, 0, stream>>>(
         static_cast<const uint16_t*>(k), gate, ape, pool_tok, pool_seq, pool_idx, n_items, block_table, max_pages,
         n_pages, k8_cache, sk_cache, status);
     return cudaGetLastError() == cudaSuccess ? KPOOL_OK : KPOOL_ERR_CUDA;
