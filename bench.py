@@ -73,7 +73,7 @@ def _peaks():
 # (dram__bytes_read.sum + dram__bytes_write.sum, T=4096 single document:
 # 308.6 + 228.6 MB / 4096 tokens), keyed by the kernel generation it was
 # taken on; another generation reports null until it is captured.
-MLA_TRAFFIC_PER_TOKEN = {"mla-tc5": 537.2e6 / 4096}
+MLA_TRAFFIC_PER_TOKEN = {"mla-tc5": 537.2e6 / 4096}     # mla-tc6: not captured yet -> null
 
 
 def _kernel_tags(K):

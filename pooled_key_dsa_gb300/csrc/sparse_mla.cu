@@ -25,7 +25,7 @@
 // Shared memory holds a 3-stage ring of 64 KB gathered blocks and two P^T tiles.
 //
 // The latent gather from L2 (about 1 KB per slot, shared by nothing across
-// queries) and the MMA chain of a block bound this kernel.  Four producer warps keep many
+// queries) and the MMA chain of a block bound this kernel.  Eight producer warps keep many
 // 16-byte cp.async in flight; each lane's copies arrive on the stage's
 // mbarrier when they land (cp.async.mbarrier.arrive.noinc), so no producer
 // ever waits for a copy, and the MMA issuers take a proxy fence before
@@ -34,10 +34,11 @@
 // the gathers of the new query's first blocks before that and prefetch the
 // next query's Q into L2, so a query boundary does not drain the ring.
 //
-// Warp roles (384 threads):
-//   warps 0-3  producers: Q rows of TMEM subpartition w, latent
-//              rows (128-byte swizzle written by hand), 16 rows of every
-//              block per warp
+// Warp roles (512 threads, per-warpgroup register budgets set with setmaxnreg):
+//   warps 0-3, 12-15  eight producers: rows 8g..8g+7 of every block for gather
+//              warp g (0-3 -> g = w, 12-15 -> g = w-8); and the Q rows of TMEM
+//              subpartition w%4, warps 0-3 latent columns 0-127, warps 12-15
+//              columns 128-255 of each half
 //   warps 4-7  softmax: lane l < 16 loads the K-half-0 row of head 16w+l and
 //              lane l+16 the K-half-1 row; a half-row exchange between the two
 //              leaves lane l with slots 0-31 and lane l+16 with slots 32-63 of
@@ -70,9 +71,10 @@ constexpr int NSTAGE = 3;              // latent-row ring depth
 constexpr int NSB = 2;                 // S / P double buffers
 constexpr int HP = 64;                 // head rows (M of S, N of PV)
 constexpr float TAU = 8.0f;            // lazy-rescale threshold (log2 units)
-constexpr int THREADS = 384;
-constexpr int NPROD = 4;               // producer warps
-constexpr int ROWS_PER_PROD = BN / NPROD;
+constexpr int THREADS = 512;
+constexpr int NPROD = 4;               // producer warps that also load Q (warps 0-3)
+constexpr int NGATH = 8;               // gather warps: 0-3 and 12-15
+constexpr int ROWS_PER_PROD = BN / NGATH;
 
 constexpr int KV_BYTES = BN * D_LAT * 2;         // 64 KB: 8 chunks x [64 rows x 128 B]
 constexpr int KV_CHUNK = BN * 128;               // 8 KB
@@ -87,7 +89,7 @@ struct Small {
     uint64_t kv_full[NSTAGE], kv_empty[NSTAGE];
     uint64_t s_full[NSB], s_free[NSB], p_full[NSB], p_empty[NSB], o_step[NSB];
     uint64_t nb_full[2], nb_empty[2];           // row-scan results, two queries deep
-    alignas(8) uint16_t mask[NSTAGE][NPROD];   // valid-slot bits, 16 slots per producer warp
+    alignas(8) uint8_t mask[NSTAGE][NGATH];    // valid-slot bits, 8 slots per gather warp
     int nbq[2];                                 // blocks of the scanned query (ring)
     int nb;
     int abort;
@@ -137,6 +139,13 @@ __device__ __forceinline__ bool wg_or(bool pred) {
     return r != 0;
 }
 
+// Per-warpgroup register budgets (launch: 512 threads x 128).  Shares: the two
+// producer warpgroups 104 each, softmax 168, issuers and row scanner 80 (sum 456).
+template <uint32_t N>
+__device__ __forceinline__ void regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(N)); }
+template <uint32_t N>
+__device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(N)); }
+
 // Warp-uniform bounded wait: lane 0 polls, every lane gets the answer.
 __device__ __forceinline__ bool warp_wait(uint32_t addr, uint32_t parity, const volatile int* abort) {
     uint32_t ok = 0;
@@ -160,17 +169,17 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
     volatile int* abort_flag = &sm.abort;
 
     if (tid == 0) {
-        tc::mbar_init(tc::smem_u32(&sm.q_full), NPROD);   // each producer warp: its Q rows stored (+ nb)
+        tc::mbar_init(tc::smem_u32(&sm.q_full), NGATH);   // each producer warp: its Q columns stored (+ nb)
         tc::mbar_init(tc::smem_u32(&sm.q_empty), 4);      // two S issuers, PV issuer, softmax
         tc::mbar_init(tc::smem_u32(&sm.o_full), 1);
         tc::mbar_init(tc::smem_u32(&sm.o_free), 4);
         tc::mbar_init(tc::smem_u32(&sm.drain), 3);
         for (int r = 0; r < 2; ++r) {
             tc::mbar_init(tc::smem_u32(&sm.nb_full[r]), 1);        // the row scanner
-            tc::mbar_init(tc::smem_u32(&sm.nb_empty[r]), NPROD);   // every producer warp has read it
+            tc::mbar_init(tc::smem_u32(&sm.nb_empty[r]), NGATH);   // every gather warp has read it
         }
         for (int s = 0; s < NSTAGE; ++s) {
-            tc::mbar_init(tc::smem_u32(&sm.kv_full[s]), NPROD * 32 + NPROD);   // copies + masks
+            tc::mbar_init(tc::smem_u32(&sm.kv_full[s]), NGATH * 32 + NGATH);   // copies + masks
             tc::mbar_init(tc::smem_u32(&sm.kv_empty[s]), 3);   // two S issuers + PV issuer
         }
         for (int b = 0; b < NSB; ++b) {
@@ -189,16 +198,19 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
     tc::fence_after();
     const uint32_t tmem = sm.tmem;
 
-    if (warp < NPROD) {
-        // ===================================================== producers
-        // Warp w: Q rows (heads 16w..16w+15) of TMEM subpartition w, and rows
-        // 16w..16w+15 of every block; lane l copies 16-byte units l and 32+l
-        // of a latent row.
+    if (warp < NPROD || warp >= 12) {
+        // ===================================================== producers (warps 0-3 also load Q)
+        regs_dec<104>();
+        const int gw = warp < NPROD ? warp : warp - 8;   // gather warp index 0..7
+        const int qc0 = warp < NPROD ? 0 : 2;            // Q column blocks 2*gw/4.. of this warp
+        // Warp w (subpartition w % 4): Q rows of heads 16(w%4)..16(w%4)+15, column blocks
+        // qc0, qc0+1 (of 4), and rows 8gw..8gw+7 of every block; lane l copies 16-byte
+        // units l and 32+l of a latent row.
         uint32_t g = 0;                             // global block counter
         uint32_t qn = 0;
         bool ok = true;
-        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-        const int qh = warp * 16 + (lane & 15);     // head whose Q row this lane stores
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        const int qh = (warp & 3) * 16 + (lane & 15);   // head whose Q row this lane stores
         const int qhalf = lane >> 4;                // latent half it stores
         for (int i = blockIdx.x; i < n_rows && ok; i += gridDim.x, ++qn) {
             if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
@@ -217,23 +229,23 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
             // the block, loaded one block ahead.
             const int pre = nb < NSTAGE - 1 ? nb : NSTAGE - 1;
             auto slot_of = [&](int b) -> int {
-                const int slot = b * BN + warp * ROWS_PER_PROD + lane;
+                const int slot = b * BN + gw * ROWS_PER_PROD + lane;
                 const int v = (lane < ROWS_PER_PROD && slot < W) ? irow[slot] : -1;
                 return (v >= 0 && v < T) ? v : -1;
             };
             int nxt = nb > 0 ? slot_of(0) : -1;
             // this lane's Q row half (512 B), loaded before the first gathers so that
             // the load latency hides behind them; stored to TMEM at b == pre
-            uint32_t qr[4][32];
+            uint32_t qr[2][32];
             {
                 const bool v = nb > 0 && qh < H;
                 const uint4* qsrc = reinterpret_cast<const uint4*>(
                     q_lat + ((int64_t)i * H + (qh < H ? qh : 0)) * D_LAT + qhalf * (D_LAT / 2));
 #pragma unroll
-                for (int c = 0; c < 4; ++c)
+                for (int c = 0; c < 2; ++c)
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
-                        const uint4 x = v ? __ldg(qsrc + c * 8 + j) : make_uint4(0u, 0u, 0u, 0u);
+                        const uint4 x = v ? __ldg(qsrc + (qc0 + c) * 8 + j) : make_uint4(0u, 0u, 0u, 0u);
                         qr[c][4 * j] = x.x;
                         qr[c][4 * j + 1] = x.y;
                         qr[c][4 * j + 2] = x.z;
@@ -246,7 +258,7 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
                     if (!warp_wait(tc::smem_u32(&sm.q_empty), (qn & 1) ^ 1, abort_flag)) { ok = false; break; }
                     if (nb > 0) {
 #pragma unroll
-                        for (int c = 0; c < 4; ++c) tc::tmem_st32(tmem + lane_base + TM_Q + 32 * c, qr[c]);
+                        for (int c = 0; c < 2; ++c) tc::tmem_st32(tmem + lane_base + TM_Q + 32 * (qc0 + c), qr[c]);
                         tc::tmem_wait_st();
                     }
                     tc::fence_before();
@@ -261,11 +273,11 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
                 if (b + 1 < nb) nxt = slot_of(b + 1);
                 const int s = g % NSTAGE;
                 if (!warp_wait(tc::smem_u32(&sm.kv_empty[s]), ((g / NSTAGE) & 1) ^ 1, abort_flag)) { ok = false; break; }
-                const uint32_t m16 = __ballot_sync(0xffffffffu, myv >= 0) & 0xffffu;
+                const uint32_t m8 = __ballot_sync(0xffffffffu, myv >= 0) & 0xffu;
                 const uint32_t dst = s_base + OFF_KV + s * KV_BYTES;
-#pragma unroll 4
+#pragma unroll
                 for (int rr = 0; rr < ROWS_PER_PROD; ++rr) {
-                    const int row = warp * ROWS_PER_PROD + rr;
+                    const int row = gw * ROWS_PER_PROD + rr;
                     const int v = __shfl_sync(0xffffffffu, myv, rr);
                     const bool valid = v >= 0;
                     const uint16_t* src = valid ? kv_lat + (int64_t)v * D_LAT : kv_lat;
@@ -277,7 +289,7 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
                 }
                 tc::cp_async_arrive_noinc(tc::smem_u32(&sm.kv_full[s]));
                 if (lane == 0) {
-                    sm.mask[s][warp] = (uint16_t)m16;
+                    sm.mask[s][gw] = (uint8_t)m8;
                     tc::mbar_arrive(tc::smem_u32(&sm.kv_full[s]));
                 }
                 ++g;
@@ -285,7 +297,9 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
         }
         tc::cp_async_wait<0>();
         if (!ok) fail(sm, status);
-    } else if (warp == 8 || warp == 9) {
+    } else if (warp >= 8 && warp < 12) {
+      regs_dec<80>();
+      if (warp == 8 || warp == 9) {
         // ===================================================== S issuers (latent half = warp - 8)
         const int half = warp - 8;
         if (lane == 0) {
@@ -409,8 +423,10 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
             __syncwarp();
         }
         if (!ok) fail(sm, status);
+      }
     } else if (warp >= 4 && warp < 8) {
         // ===================================================== softmax / correction / epilogue
+        regs_inc<168>();
         // Row h = 16*wid + (lane & 15) (head); lane half hs = lane >> 4 owns
         // slots 32*hs .. 32*hs+31 of the block.  `bad` is sticky per thread and
         // ORed across the four warps at every named barrier (bar.red.or).
