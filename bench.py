@@ -70,10 +70,10 @@ def _peaks():
 
 
 # DRAM bytes per query token of the sparse MLA kernel from an ncu capture
-# (dram__bytes_read.sum + dram__bytes_write.sum, T=4096 single document:
-# 308.6 + 228.6 MB / 4096 tokens), keyed by the kernel generation it was
-# taken on; another generation reports null until it is captured.
-MLA_TRAFFIC_PER_TOKEN = {"mla-tc5": 537.2e6 / 4096}     # mla-tc6: not captured yet -> null
+# (dram__bytes_read.sum + dram__bytes_write.sum, T=4096 single document), keyed
+# by the kernel generation it was taken on; another generation reports null
+# until it is captured.
+MLA_TRAFFIC_PER_TOKEN = {"mla-tc5": 537.2e6 / 4096, "mla-tc6": (309.190144e6 + 227.536640e6) / 4096}
 
 
 def _kernel_tags(K):
