@@ -104,6 +104,24 @@ def _work(wl):
     }
 
 
+# ----------------------------------------------------------------- ranks
+
+def max_over_ranks(value: float, world: int, device) -> float:
+    """The largest value over the ranks (a job's time is that of its slowest rank); one
+    all-reduce when world > 1 (NCCL for CUDA tensors, any backend for CPU tensors)."""
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, units_per_rank: int, steps: int, total_ms: float) -> float:
+    """Whole-job units per second: every rank processes units_per_rank per step (weak scaling)."""
+    return world * units_per_rank * steps / (total_ms / 1e3)
+
+
 # ----------------------------------------------------------------- clocks
 
 class ClockSampler:
@@ -551,12 +569,8 @@ def main():
         "dsa_index": statistics.mean(e[1].elapsed_time(e[6]) for e in ev),
         "sparse_mla": statistics.mean(e[6].elapsed_time(e[7]) for e in ev),
     }
-    total_ms = sum(step_ms)
-    tmax = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(tmax, op=dist.ReduceOp.MAX)
-    total_ms = float(tmax.item())
-    value = world * T * a.steps / (total_ms / 1e3)
+    total_ms = max_over_ranks(sum(step_ms), world, dev)
+    value = job_throughput(world, T, a.steps, total_ms)
 
     # ---- end to end through the public API with host buffers: kpool_forward_host moves the inputs from
     # page-locked host memory and the outputs back, overlapping the copies of query-row blocks with the kernels
@@ -603,11 +617,8 @@ def main():
     bwd = run_bwd(a, wl, K, dev, d["q_lat"], d["kv_lat"], idx, out, lse, _work(wl)["valid_slots"], flush)
     # ---- a paged decode step (its own workload)
     dec = run_decode(a, K, dev, flush)
-    e2e_ms = sum(x.elapsed_time(y) for x, y in e2e_ev)
-    tm = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        dist.all_reduce(tm, op=dist.ReduceOp.MAX)
-    e2e_value = world * T * a.steps / (float(tm.item()) / 1e3)
+    e2e_ms = max_over_ranks(sum(x.elapsed_time(y) for x, y in e2e_ev), world, dev)
+    e2e_value = job_throughput(world, T, a.steps, e2e_ms)
 
     if rank != 0:
         if world > 1:
