@@ -164,21 +164,37 @@ __device__ void select_registers(SelectSmem& s, const float* __restrict__ sc, in
         key[j] = p < n ? score_key(sc[p]) : 0u;
         valid |= (p < n ? 1u : 0u) << j;
     }
+    // Radix levels over bits 31..21, 20..10, 9..0.  When the bin that holds the
+    // topk-th key is kept whole (its count equals the keys still needed), every
+    // key from the bin's lowest value up is kept and the later levels are skipped.
     fast_level(s, key, valid, 0u, 0u, 21, 2048, (uint32_t)topk);
     uint32_t prefix = s.digit << 21;
-    fast_level(s, key, valid, 0xFFE00000u, prefix, 10, 2048, s.remaining);
-    prefix |= s.digit << 10;
-    fast_level(s, key, valid, 0xFFFFFC00u, prefix, 0, 1024, s.remaining);
-    const uint32_t K = prefix | s.digit;
-    const uint32_t need_eq = s.remaining;
-    const uint32_t n_eq = s.hist[s.digit & 1023u];   // keys equal to K
-    __syncthreads();
+    uint32_t rem = s.remaining, cnt = s.hist[s.digit & 2047u];
+    __syncthreads();                                 // every thread has read the bin before it is reused
+    bool whole = cnt == rem;
+    if (!whole) {
+        fast_level(s, key, valid, 0xFFE00000u, prefix, 10, 2048, rem);
+        prefix |= s.digit << 10;
+        rem = s.remaining;
+        cnt = s.hist[s.digit & 2047u];
+        __syncthreads();
+        whole = cnt == rem;
+    }
+    uint32_t K = prefix, need_eq = 0, n_eq = 0;      // whole bin: keep every key >= K
+    if (!whole) {
+        fast_level(s, key, valid, 0xFFFFFC00u, prefix, 0, 1024, rem);
+        K = prefix | s.digit;
+        need_eq = s.remaining;
+        n_eq = s.hist[s.digit & 1023u];              // keys equal to K
+        __syncthreads();
+    }
 
     uint32_t gt = 0, eq = 0;
 #pragma unroll
     for (int j = 0; j < NC; ++j) {
-        gt |= (((valid >> j) & 1u) && key[j] > K ? 1u : 0u) << j;
-        eq |= (((valid >> j) & 1u) && key[j] == K ? 1u : 0u) << j;
+        const bool v = (valid >> j) & 1u;
+        gt |= (v && (whole ? key[j] >= K : key[j] > K) ? 1u : 0u) << j;
+        eq |= (v && !whole && key[j] == K ? 1u : 0u) << j;
     }
     uint32_t take = gt | eq;
     uint32_t bal[NC];
