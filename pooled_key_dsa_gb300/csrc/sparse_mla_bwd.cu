@@ -39,12 +39,14 @@
 // With the gather (1 KB per slot in) these reductions (2 KB per slot out) make
 // the SM's traffic with L2 the bound.
 //
-// Warp roles (480 threads):
+// Warp roles (640 threads, per-warpgroup register budgets set with setmaxnreg):
 //   warps 0-3   producers: the Q / dO rows of subpartition w, 8 latent rows
 //               of every block (cp.async, completion counted on mbarriers)
 //   warps 4-7   P / dZ' (one head per lane pair, 16 slots per lane), and the
 //               dQ epilogue of each query
-//   warps 8-11  dKv scatter (one latent row of a tile per thread)
+//   warps 8-11  dKv scatter of the tiles in TMEM buffer 0 (latent tiles 0, 2)
+//   warps 16-19 dKv scatter of the tiles in TMEM buffer 1 (latent tiles 1, 3);
+//               one latent row of a tile per thread
 //   warp 12     [S; dP] issuer (and TMEM owner)
 //   warp 13     dQ^T / dKv^T issuer
 //   warp 14     row scanner: block count and range check of each index row,
@@ -64,7 +66,7 @@ namespace {
 constexpr int BN = 32;                 // slots per gathered block
 constexpr int NSTAGE = 2;              // gathered-block ring
 constexpr int HP = 64;                 // head rows
-constexpr int THREADS = 480;
+constexpr int THREADS = 640;
 constexpr int NPROD = 4;
 constexpr int ROWS_PER_PROD = BN / NPROD;
 constexpr int QD_CHUNK = 128 * 128;    // 16 KB: 128 stacked rows x 128 B (64 bf16 of the latent)
@@ -99,7 +101,14 @@ constexpr uint32_t ID_DQ = tc::idesc(128, HP, 1, 1, true, false);
 constexpr uint32_t ID_DK = tc::idesc(128, 2 * BN, 1, 1, true, true);
 
 constexpr uint32_t COPY_ARRIVALS = NPROD * 32 + NPROD;   // copies + one explicit arrive per warp
-constexpr uint32_t QD_RELEASES = 2 + 4 + 4;              // two issuers, four P/dZ warps, four scatter warps
+constexpr uint32_t QD_RELEASES = 2 + 4 + 8;              // two issuers, four P/dZ warps, eight scatter warps
+
+// Per-warpgroup register budgets (launch: 640 threads x 96): producers 40, P/dZ 120, two
+// scatter groups 112 each, issuers and row scanner 88 -- 472 of the 480 per thread-quintet.
+template <uint32_t N>
+__device__ __forceinline__ void regs_inc() { asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(N)); }
+template <uint32_t N>
+__device__ __forceinline__ void regs_dec() { asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(N)); }
 
 __device__ __forceinline__ uint32_t swz(int row, int unit) { return (uint32_t)(row * 128 + ((unit ^ (row & 7)) << 4)); }
 
@@ -183,6 +192,7 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_bwd_kernel(
 
     if (warp < NPROD) {
         // ===================================================== producers
+        regs_dec<40>();
         uint32_t g = 0, qn = 0;
         bool ok = true;
         for (int i = blockIdx.x; i < n_rows && ok; i += gridDim.x, ++qn) {
@@ -237,7 +247,9 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_bwd_kernel(
         }
         tc::cp_async_wait<0>();
         if (!ok) fail(sm, status);
-    } else if (warp == 12) {
+    } else if (warp >= 12 && warp < 16) {
+      regs_dec<88>();
+      if (warp == 12) {
         // ===================================================== [S; dP] issuer
         if (lane == 0) {
             uint32_t g = 0, qn = 0;
@@ -374,8 +386,10 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_bwd_kernel(
             __syncwarp();
         }
         if (!ok) fail(sm, status);
+      }
     } else if (warp >= 4 && warp < 8) {
         // ===================================================== P / dZ' and the dQ epilogue
+        regs_inc<120>();
         // Lane pair (l, l+16) owns head h = 16*sp + l; lane half hs owns slots 16hs .. 16hs+15 of a block.
         const int sp = warp - 4;
         const int hs = lane >> 4;
@@ -481,11 +495,13 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_bwd_kernel(
             if (lane == 0) tc::mbar_arrive(tc::smem_u32(&sm.dq_free));
         }
         if (bad) fail(sm, status);
-    } else if (warp >= 8 && warp < 12) {
-        // ===================================================== dKv scatter
+    } else {
+        // ===================================================== dKv scatter (warps 8-11: tiles 0, 2; 16-19: tiles 1, 3)
+        regs_inc<112>();
         // Thread (subpartition sp, lane l) holds latent row d = 128t + 32sp + l of the dKv^T tile
         // t for the pair's 64 slots; a warp's reduction covers 128 contiguous bytes of one kv row.
-        const int sp = warp - 8;
+        const int sp = warp & 3;
+        const int grp = warp >= 16 ? 1 : 0;           // TMEM buffer (and tile parity) of this group
         const uint32_t lane_base = (uint32_t)(sp * 32) << 16;
         uint32_t qn = 0, c = 0;
         bool bad = false;
@@ -504,6 +520,7 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_bwd_kernel(
                 r1 = (r1 >= 0 && r1 < T) ? r1 : -1;
                 for (int t = 0; t < 4; ++t, ++c) {
                     const int kb = c & 1;
+                    if (kb != grp) continue;
                     if (!warp_wait(tc::smem_u32(&sm.dk_full[kb]), (c >> 1) & 1, abort_flag)) { bad = true; break; }
                     tc::fence_after();
                     uint32_t v0[32], v1[32];
