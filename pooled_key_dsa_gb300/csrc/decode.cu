@@ -125,106 +125,152 @@ __global__ void __launch_bounds__(128) paged_append_kernel(
 }
 
 // ---------------------------------------------------------------- paged scoring
-// One CTA per (128-pool tile, sequence): the tile's 4 pages of codes (TMA, 4 KB
-// each) are the M = 128 operand, the query's H_i rows of codes the N = H_i
-// operand; 4 tcgen05 kind::f8f6f4 MMAs (K = 32 each) accumulate the head dots
-// in TMEM; thread t of the 128 then owns pool 128*tile + t: ReLU, the head
-// weights ws, the pool scale.  Scores of row b go to scores[b * stride + p].
+// One CTA per (group of DS_TILES 128-pool tiles, sequence).  All the group's
+// pages of codes (TMA, 4 KB each; a tile's 4 pages are the M = 128 operand) and
+// the query's H_i rows of codes (the N = H_i operand) are requested at once,
+// one barrier per tile; warp 4 issues each tile's 4 tcgen05 kind::f8f6f4 MMAs
+// (K = 32 each) into that tile's own TMEM accumulator as soon as its pages
+// land, so the loads of later tiles, the MMAs and the epilogue of earlier ones
+// overlap.  Epilogue: thread t of warps 0-3 owns pool 128*tile + t: ReLU, the
+// head weights ws, the pool scale.  Scores of row b go to scores[b * stride + p].
 namespace {
 
+constexpr int DS_TILES = 4;                        // 128-pool tiles per CTA
+constexpr int DS_THREADS = 160;                    // warps 0-3 epilogue, warp 4 TMA + MMA
+constexpr int DS_A_BYTES = 128 * 128;
+
 struct DsSmall {
-    uint64_t full, done;
+    uint64_t q_full, full[DS_TILES], done[DS_TILES], drain;
     uint32_t tmem;
-    int abort;                                     // never raised: a CTA has nobody to wait for but itself
+    int abort;
 };
+template <int HI>
+constexpr int ds_smem() { return DS_TILES * DS_A_BYTES + HI * 128 + (int)sizeof(DsSmall) + 1024; }
 
 template <int HI>
-__global__ void __launch_bounds__(128) decode_score_kernel(const __grid_constant__ CUtensorMap map_q,
-                                                           const __grid_constant__ CUtensorMap map_k,
-                                                           const float* __restrict__ ws,
-                                                           const float* __restrict__ sk_cache,
-                                                           const int32_t* __restrict__ block_table, int max_pages,
-                                                           int n_pages, const int32_t* __restrict__ seq_lens,
-                                                           float* __restrict__ scores, int64_t stride,
-                                                           int32_t* status) {
-    __shared__ __align__(1024) uint8_t a_tile[128 * 128];
-    __shared__ __align__(1024) uint8_t b_tile[HI * 128];
-    __shared__ DsSmall sm;
-    __shared__ float wsh[HI];
+__global__ void __launch_bounds__(DS_THREADS) decode_score_kernel(const __grid_constant__ CUtensorMap map_q,
+                                                                  const __grid_constant__ CUtensorMap map_k,
+                                                                  const float* __restrict__ ws,
+                                                                  const float* __restrict__ sk_cache,
+                                                                  const int32_t* __restrict__ block_table,
+                                                                  int max_pages, int n_pages,
+                                                                  const int32_t* __restrict__ seq_lens,
+                                                                  float* __restrict__ scores, int64_t stride,
+                                                                  int32_t* status) {
+    extern __shared__ __align__(1024) uint8_t ds_raw[];
+    uint8_t* smem = ds_raw + ((1024u - (tc::smem_u32(ds_raw) & 1023u)) & 1023u);
+    uint8_t* a_tiles = smem;
+    uint8_t* b_tile = smem + DS_TILES * DS_A_BYTES;
+    DsSmall& sm = *reinterpret_cast<DsSmall*>(b_tile + HI * 128);
+    __shared__ __align__(16) float wsh[HI];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int b = blockIdx.y, tile = blockIdx.x;
+    const int b = blockIdx.y, tile0 = blockIdx.x * DS_TILES;
     const int L = seq_lens[b];
     if (L > max_pages * PAGE_TOKENS) {                // the block table cannot hold the sequence
-        if (tile == 0 && threadIdx.x == 0) set_status(status, KPOOL_ERR_SHAPE);
+        if (blockIdx.x == 0 && threadIdx.x == 0) set_status(status, KPOOL_ERR_SHAPE);
         return;
     }
     const int n = L / KPOOL;                          // complete pools of the sequence
-    if (tile * 128 >= n) return;
-    const int npg = min(4, (n - tile * 128 + PAGE_POOLS - 1) / PAGE_POOLS);   // pages of this tile
+    if (tile0 * 128 >= n) return;
+    const int nt = min(DS_TILES, (n - tile0 * 128 + 127) / 128);   // tiles of this CTA
     if (tid < HI) wsh[tid] = ws[(int64_t)b * HI + tid];
-    if (tid == 0) {
-        tc::mbar_init(tc::smem_u32(&sm.full), 1);
-        tc::mbar_init(tc::smem_u32(&sm.done), 1);
+    if (tid == 128) {
+        tc::mbar_init(tc::smem_u32(&sm.q_full), 1);
+        for (int j = 0; j < DS_TILES; ++j) {
+            tc::mbar_init(tc::smem_u32(&sm.full[j]), 1);
+            tc::mbar_init(tc::smem_u32(&sm.done[j]), 1);
+        }
+        tc::mbar_init(tc::smem_u32(&sm.drain), 1);
         sm.abort = 0;
         tc::mbar_init_fence();
     }
-    if (warp == 0) tc::tmem_alloc(tc::smem_u32(&sm.tmem), 32);
+    if (warp == 4) tc::tmem_alloc(tc::smem_u32(&sm.tmem), 128);
     tc::fence_before();
     __syncthreads();
     tc::fence_after();
     const uint32_t tmem = sm.tmem;
-    bool ok = true;
-    if (tid == 0) {
-        tc::mbar_arrive_expect_tx(tc::smem_u32(&sm.full), (uint32_t)(npg * PAGE_POOLS * 128 + HI * 128));
-        for (int j = 0; j < npg; ++j) {
-            const int page = block_table[(int64_t)b * max_pages + tile * 4 + j];
-            tc::tma_load_2d(tc::smem_u32(a_tile + j * PAGE_POOLS * 128), &map_k, 0, page * PAGE_POOLS,
-                            tc::smem_u32(&sm.full));
-        }
-        tc::tma_load_2d(tc::smem_u32(b_tile), &map_q, 0, b * HI, tc::smem_u32(&sm.full));
-        ok = tc::mbar_wait(tc::smem_u32(&sm.full), 0, &sm.abort);
-        if (ok) {
-            tc::fence_after();
-            const uint64_t ad = tc::sw128_desc(tc::smem_u32(a_tile), 0, 1024);
+    volatile int* abort_flag = &sm.abort;
+
+    if (warp == 4) {
+        if (lane == 0) {
+            tc::mbar_arrive_expect_tx(tc::smem_u32(&sm.q_full), (uint32_t)(HI * 128));
+            tc::tma_load_2d(tc::smem_u32(b_tile), &map_q, 0, b * HI, tc::smem_u32(&sm.q_full));
+            for (int j = 0; j < nt; ++j) {
+                const int tile = tile0 + j;
+                const int npg = min(4, (n - tile * 128 + PAGE_POOLS - 1) / PAGE_POOLS);   // pages of this tile
+                tc::mbar_arrive_expect_tx(tc::smem_u32(&sm.full[j]), (uint32_t)(npg * PAGE_POOLS * 128));
+                for (int g = 0; g < npg; ++g) {
+                    const int page = block_table[(int64_t)b * max_pages + tile * 4 + g];
+                    // an out-of-range page id reads TMA's zero fill; the epilogue flags it
+                    tc::tma_load_2d(tc::smem_u32(a_tiles + j * DS_A_BYTES + g * PAGE_POOLS * 128), &map_k, 0,
+                                    page * PAGE_POOLS, tc::smem_u32(&sm.full[j]));
+                }
+            }
+            bool ok = tc::mbar_wait(tc::smem_u32(&sm.q_full), 0, abort_flag);
             const uint64_t bd = tc::sw128_desc(tc::smem_u32(b_tile), 0, 1024);
             constexpr uint32_t id = tc::idesc(128, HI, 0, 0, false, false);
+            for (int j = 0; ok && j < nt; ++j) {
+                ok = tc::mbar_wait(tc::smem_u32(&sm.full[j]), 0, abort_flag);
+                if (!ok) break;
+                tc::fence_after();
+                const uint64_t ad = tc::sw128_desc(tc::smem_u32(a_tiles + j * DS_A_BYTES), 0, 1024);
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-                tc::mma_e4m3(tmem, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), id, kk > 0 ? 1u : 0u);
-            tc::commit(tc::smem_u32(&sm.done));
-            ok = tc::mbar_wait(tc::smem_u32(&sm.done), 0, &sm.abort);
+                for (int kk = 0; kk < 4; ++kk)
+                    tc::mma_e4m3(tmem + 32 * j, ad + (uint64_t)(kk * 2), bd + (uint64_t)(kk * 2), id,
+                                 kk > 0 ? 1u : 0u);
+                tc::commit(tc::smem_u32(&sm.done[j]));
+            }
+            if (!ok) {
+                sm.abort = 1;                          // the epilogue stops waiting
+                set_status(status, KPOOL_ERR_TIMEOUT);
+            }
+            // every MMA issued has completed before TMEM is released
+            tc::commit(tc::smem_u32(&sm.drain));
+            const uint64_t t0 = tc::globaltimer_ns();
+            while (!tc::mbar_try(tc::smem_u32(&sm.drain), 0) && tc::globaltimer_ns() - t0 < tc::WAIT_LIMIT_NS) {
+            }
         }
-        if (!ok) {
-            sm.tmem = 0xffffffffu;                   // signals the epilogue to skip
-            set_status(status, KPOOL_ERR_TIMEOUT);
-        }
-    }
-    __syncthreads();
-    tc::fence_after();
-    if (sm.tmem != 0xffffffffu) {
-        // thread t: TMEM lane t = pool 128*tile + t; columns = heads
-        uint32_t acc[32];
-        tc::tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16), acc);
-        tc::tmem_wait_ld();
-        float s = 0.f;
+        __syncwarp();
+    } else {
+        // thread t: TMEM lane t = pool 128*tile + t; columns 32j .. 32j + HI - 1 = heads of tile j
+        for (int j = 0; j < nt; ++j) {
+            const int p = (tile0 + j) * 128 + tid;
+            const int page = p < n ? block_table[(int64_t)b * max_pages + (p / PAGE_POOLS)] : -1;
+            const bool page_ok = page >= 0 && page < n_pages;
+            const float sk = page_ok ? sk_cache[(int64_t)page * PAGE_POOLS + (p % PAGE_POOLS)] : 0.f;
+            uint32_t ok = 0;
+            if (lane == 0) ok = tc::mbar_wait(tc::smem_u32(&sm.done[j]), 0, abort_flag) ? 1u : 0u;
+            if (__shfl_sync(0xffffffffu, ok, 0) == 0) break;
+            tc::fence_after();
+            uint32_t acc[32];
+            tc::tmem_ld32(tmem + 32 * j + ((uint32_t)(warp * 32) << 16), acc);
+            tc::tmem_wait_ld32(acc);
+            float2 part[4];
 #pragma unroll
-        for (int h = 0; h < HI; ++h) s += wsh[h] * fmaxf(__uint_as_float(acc[h]), 0.f);
-        const int p = tile * 128 + tid;
-        if (p < n) {
-            const int page = block_table[(int64_t)b * max_pages + (p / PAGE_POOLS)];
-            if (page >= 0 && page < n_pages) {
-                scores[(int64_t)b * stride + p] = s * sk_cache[(int64_t)page * PAGE_POOLS + (p % PAGE_POOLS)];
-            } else {
-                scores[(int64_t)b * stride + p] = -INFINITY;
-                set_status(status, KPOOL_ERR_INDEX_RANGE);
+            for (int h = 0; h < HI; h += 2) {
+                const float2 x = make_float2(fmaxf(__uint_as_float(acc[h]), 0.f),
+                                             fmaxf(__uint_as_float(acc[h + 1]), 0.f));
+                const float2 w2 = make_float2(wsh[h], wsh[h + 1]);
+                if (h < 8) part[h / 2] = __fmul2_rn(x, w2);
+                else part[(h / 2) & 3] = __ffma2_rn(x, w2, part[(h / 2) & 3]);
+            }
+            part[0] = __fadd2_rn(__fadd2_rn(part[0], part[1]), __fadd2_rn(part[2], part[3]));
+            const float s = part[0].x + part[0].y;
+            if (p < n) {
+                if (page_ok) {
+                    scores[(int64_t)b * stride + p] = s * sk;
+                } else {
+                    scores[(int64_t)b * stride + p] = -INFINITY;
+                    set_status(status, KPOOL_ERR_INDEX_RANGE);
+                }
             }
         }
     }
     tc::fence_before();
     __syncthreads();
-    if (warp == 0) {
+    if (warp == 4) {
         tc::fence_after();
-        tc::tmem_dealloc(tmem, 32);
+        tc::tmem_dealloc(tmem, 128);
     }
 }
 
@@ -248,9 +294,18 @@ int launch_ds(const uint8_t* q8, const float* ws, const uint8_t* k8_cache, const
     if (!make_u8_map(&mq, q8, (uint64_t)B * HI, HI) ||
         !make_u8_map(&mk, k8_cache, (uint64_t)n_pages * PAGE_POOLS, PAGE_POOLS))
         return KPOOL_ERR_CUDA;
-    const dim3 grid((unsigned)((max_pages + 3) / 4), (unsigned)B);
-    decode_score_kernel<HI><<<grid, 128, 0, stream>>>(mq, mk, ws, sk_cache, block_table, max_pages, n_pages, seq_lens,
-                                                      scores, stride, status);
+    static bool attr[64] = {false};                   // per device: the shared-memory opt-in is set
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return KPOOL_ERR_CUDA;
+    if (!attr[dev]) {
+        if (cudaFuncSetAttribute(decode_score_kernel<HI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 ds_smem<HI>()) != cudaSuccess)
+            return KPOOL_ERR_CUDA;
+        attr[dev] = true;
+    }
+    const dim3 grid((unsigned)((max_pages + 4 * DS_TILES - 1) / (4 * DS_TILES)), (unsigned)B);
+    decode_score_kernel<HI><<<grid, DS_THREADS, ds_smem<HI>(), stream>>>(mq, mk, ws, sk_cache, block_table, max_pages,
+                                                                       n_pages, seq_lens, scores, stride, status);
     return cudaGetLastError() == cudaSuccess ? KPOOL_OK : KPOOL_ERR_CUDA;
 }
 

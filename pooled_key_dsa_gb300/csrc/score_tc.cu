@@ -14,9 +14,12 @@
 // pools, N = 256, K = 32) into one of two TMEM accumulators, so the epilogue
 // of tile t overlaps the MMAs of tile t+1.
 //
-// Epilogue: 8 warps, two per TMEM subpartition; a thread owns one pool (its
-// TMEM lane) and half of the columns, so ReLU, the head weights and the head
-// sum stay thread-local; one coalesced store per (query, pool).
+// Epilogue: two groups of 4 warps; group g takes the tiles of TMEM buffer g,
+// so the epilogues of consecutive tiles run side by side.  A thread owns one
+// pool (its TMEM lane) and all 256 columns, read in 32-column loads issued one
+// chunk ahead; ReLU, the head weights and the head sum stay thread-local
+// (packed fp32 FMAs, independent partial sums); one coalesced store per
+// (query, pool).
 // Items are spread over the persistent CTAs in a snake order (the item size
 // grows along a document).  Waits are bounded (KPOOL_ERR_TIMEOUT).
 #include <cstdint>
@@ -39,7 +42,7 @@ constexpr int B_BYTES = 256 * 128;     // 256 (query, head) rows x 128 B
 constexpr int OFF_B = 0;
 constexpr int OFF_A = OFF_B + 2 * B_BYTES;
 constexpr int OFF_WS = OFF_A + A_STAGES * A_BYTES;
-constexpr int OFF_SMALL = OFF_WS + 2 * 256 * 4;
+constexpr int OFF_SMALL = OFF_WS + 4 * 256 * 4;     // two groups x two items x 256 weights
 
 struct ScSmall {
     uint64_t b_full[2], b_empty[2], a_full[A_STAGES], a_empty[A_STAGES], acc_full[2], acc_empty[2], drain;
@@ -85,15 +88,51 @@ __device__ __forceinline__ bool warp_wait(uint32_t addr, uint32_t parity, const 
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
-// Named barrier 1 over the 256 epilogue threads, ORing a predicate.
-__device__ __forceinline__ bool epi_or(bool pred) {
+// Named barrier 1 + g over the 128 threads of epilogue group g, ORing a predicate.
+__device__ __forceinline__ bool group_or(bool pred, int g) {
     uint32_t r;
     asm volatile(
-        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, 1, 256, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+        "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, %2, 128, p;\n selp.u32 %0, 1, 0, q;\n}\n"
         : "=r"(r)
-        : "r"((uint32_t)pred)
+        : "r"((uint32_t)pred), "r"(1 + g)
         : "memory");
     return r != 0;
+}
+
+// One 32-column chunk cc of a thread's row (cc is a constant after unrolling):
+// res[q] = sum over the heads h of query q in this chunk of
+// ws[q,h] * ReLU(acc[q,h]).  Column pairs go through packed fp32 FMAs into up
+// to four independent partial sums per query (short dependency chains); a
+// query spanning two chunks (H_i = 64) adds the second chunk's sum to the first.
+template <int HI, int NQ>
+__device__ __forceinline__ void score_chunk(const uint32_t (&v)[32], const float* __restrict__ wrow, int cc,
+                                            float (&res)[NQ]) {
+    constexpr int HC = HI >= 32 ? 32 : HI;           // columns of one query in this chunk
+    constexpr int QPC = 32 / HC;                     // queries in this chunk
+    constexpr int PPQ = HC / 2;                      // column pairs of one query
+    constexpr int NP = PPQ >= 4 ? 4 : PPQ;           // partial sums per query
+    const float4* w4 = reinterpret_cast<const float4*>(wrow + cc * 32);
+#pragma unroll
+    for (int qq = 0; qq < QPC; ++qq) {
+        float2 part[NP];
+#pragma unroll
+        for (int jp = 0; jp < PPQ; ++jp) {
+            const int c = qq * HC + 2 * jp;           // column within the chunk
+            const float4 wv = w4[c >> 2];
+            const float2 w2 = (c & 2) ? make_float2(wv.z, wv.w) : make_float2(wv.x, wv.y);
+            const float2 x = make_float2(fmaxf(__uint_as_float(v[c]), 0.f), fmaxf(__uint_as_float(v[c + 1]), 0.f));
+            if (jp < NP)
+                part[jp] = __fmul2_rn(x, w2);
+            else
+                part[jp % NP] = __ffma2_rn(x, w2, part[jp % NP]);
+        }
+#pragma unroll
+        for (int p = 1; p < NP; ++p) part[0] = __fadd2_rn(part[0], part[p]);
+        const int q = cc * 32 / HI + qq;
+        const float s = part[0].x + part[0].y;
+        if ((cc * 32) % HI == 0) res[q] = s;
+        else res[q] += s;
+    }
 }
 
 }  // namespace
@@ -118,7 +157,7 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_tc_kernel(
             tc::mbar_init(tc::smem_u32(&sm.b_full[b]), 1);
             tc::mbar_init(tc::smem_u32(&sm.b_empty[b]), 1);
             tc::mbar_init(tc::smem_u32(&sm.acc_full[b]), 1);
-            tc::mbar_init(tc::smem_u32(&sm.acc_empty[b]), 8);
+            tc::mbar_init(tc::smem_u32(&sm.acc_empty[b]), 4);
         }
         for (int s = 0; s < A_STAGES; ++s) {
             tc::mbar_init(tc::smem_u32(&sm.a_full[s]), 1);
@@ -208,9 +247,11 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_tc_kernel(
         __syncwarp();
     } else if (warp >= 4) {
         // ===================================================== epilogue
-        const int e = tid - 128;                      // 0..255
+        // group g (warps 4-7 / 8-11) takes the tiles of TMEM buffer g (running tile index of parity g), so
+        // the epilogues of two consecutive tiles run at once; warp w reads TMEM lanes 32*(w%4) .., all columns
+        const int g = (warp - 4) >> 2;
+        const int e = tid - 128 - 128 * g;            // 0..127 within the group
         const int sp = warp & 3;                      // TMEM subpartition (lanes 32sp..)
-        const int ch = (warp - 4) >> 2;               // column half: queries ch*QG/2 ..
         const uint32_t lane_base = (uint32_t)(sp * 32) << 16;
         uint32_t ni = 0, nacc = 0;
         bool bad = false;
@@ -219,44 +260,82 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_tc_kernel(
             if (j >= total) break;
             const Item it = decode_item(j, sched, cu_seqlens, cu_pools, n_docs, topk, QG);
             const int i0 = it.s_d + it.r0;
-            // the item's head weights (256 floats) into shared memory
-            float* wsb = reinterpret_cast<float*>(smem + OFF_WS) + (ni & 1) * 256;
+            // the item's head weights (256 floats) into this group's shared buffer
+            float* wsb = reinterpret_cast<float*>(smem + OFF_WS) + g * 512 + (ni & 1) * 256;
             wsb[e] = (it.r0 + e / HI < it.L) ? ws[(int64_t)i0 * HI + e] : 0.f;
-            if (epi_or(bad)) { bad = true; break; }
+            wsb[e + 128] = (it.r0 + (e + 128) / HI < it.L) ? ws[(int64_t)i0 * HI + e + 128] : 0.f;
+            if (group_or(bad, g)) { bad = true; break; }
             const int64_t row_base = pair_base[it.d];
-            for (int t = 0; t < it.ntiles; ++t, ++nacc) {
-                const int ab = nacc & 1;
-                bad = bad || !warp_wait(tc::smem_u32(&sm.acc_full[ab]), (nacc >> 1) & 1, abort_flag);
-                if (bad) continue;
-                tc::fence_after();
+            // per query: the start of its score row and its pool count (0: no scored row)
+            constexpr int QS = QG <= 8 ? QG : 1;
+            int64_t qbase[QS];
+            int qlim[QS];
+            if constexpr (QG <= 8) {
+#pragma unroll
+                for (int q = 0; q < QG; ++q) {
+                    const int r = it.r0 + q;
+                    const int n_i = (r + 1) / KPOOL;
+                    qbase[q] = row_base + pairs_before(r);
+                    qlim[q] = (r < it.L && n_i > topk) ? n_i : 0;
+                }
+            }
+            for (int t = (int)((nacc & 1) != (uint32_t)g); t < it.ntiles; t += 2) {
+                const uint32_t na = nacc + (uint32_t)t;      // running tile index; buffer na & 1 == g
                 const int pool_local = 128 * t + 32 * sp + lane;
                 const int pool = it.p0 + pool_local;
                 const float sk = pool < max_pools ? s_k[pool] : 0.f;
-                float acc[QG / 2];
+                bad = bad || !warp_wait(tc::smem_u32(&sm.acc_full[g]), (na >> 1) & 1, abort_flag);
+                if (bad) continue;                           // the group learns it at the next item
+                tc::fence_after();
+                // eight 32-column loads; each is issued before the previous chunk is summed
+                const uint32_t tb = tmem + 256 * g + lane_base;
+                float res[QG];
+                auto store = [&](int q) {
+                    if constexpr (QG <= 8) {
+                        if (pool_local < qlim[q]) scores[qbase[q] + pool_local] = res[q] * sk;
+                    } else {
+                        const int r = it.r0 + q;
+                        const int n_i = (r + 1) / KPOOL;
+                        if (r < it.L && n_i > topk && pool_local < n_i)
+                            scores[row_base + pairs_before(r) + pool_local] = res[q] * sk;
+                    }
+                };
+                if constexpr (QG <= 32) {
+                    uint32_t v[2][32];
+                    tc::tmem_ld32(tb, v[0]);
+                    tc::tmem_wait_ld32(v[0]);
 #pragma unroll
-                for (int q = 0; q < QG / 2; ++q) acc[q] = 0.f;
+                    for (int cc = 0; cc < 8; ++cc) {
+                        if (cc < 7) {
+                            tc::tmem_ld32(tb + 32 * (cc + 1), v[(cc + 1) & 1]);
+                        } else {                              // every load of the buffer has completed
+                            tc::fence_before();
+                            __syncwarp();
+                            if (lane == 0) tc::mbar_arrive(tc::smem_u32(&sm.acc_empty[g]));
+                        }
+                        score_chunk<HI>(v[cc & 1], wsb, cc, res);
+                        if (cc < 7) tc::tmem_wait_ld32(v[(cc + 1) & 1]);
+                    }
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
+                    for (int q = 0; q < QG; ++q) store(q);
+                } else {                                      // H_i = 4: 64 results per thread, one buffer
                     uint32_t v[32];
-                    tc::tmem_ld32(tmem + 256 * ab + lane_base + ch * 128 + cc * 32, v);
-                    tc::tmem_wait_ld();
 #pragma unroll
-                    for (int jj = 0; jj < 32; ++jj) {
-                        const int col = ch * 128 + cc * 32 + jj;                 // (query, head) column
-                        acc[(cc * 32 + jj) / HI] += wsb[col] * fmaxf(__uint_as_float(v[jj]), 0.f);
+                    for (int cc = 0; cc < 8; ++cc) {
+                        tc::tmem_ld32(tb + 32 * cc, v);
+                        tc::tmem_wait_ld32(v);
+                        if (cc == 7) {
+                            tc::fence_before();
+                            __syncwarp();
+                            if (lane == 0) tc::mbar_arrive(tc::smem_u32(&sm.acc_empty[g]));
+                        }
+                        score_chunk<HI>(v, wsb, cc, res);
+#pragma unroll
+                        for (int q = cc * QG / 8; q < (cc + 1) * QG / 8; ++q) store(q);   // queries of chunk cc
                     }
                 }
-                tc::fence_before();
-                __syncwarp();
-                if (lane == 0) tc::mbar_arrive(tc::smem_u32(&sm.acc_empty[ab]));
-#pragma unroll
-                for (int q = 0; q < QG / 2; ++q) {
-                    const int r = it.r0 + ch * (QG / 2) + q;
-                    const int n_i = (r + 1) / KPOOL;
-                    if (r < it.L && n_i > topk && pool_local < n_i)
-                        scores[row_base + pairs_before(r) + pool_local] = acc[q] * sk;
-                }
             }
+            nacc += (uint32_t)it.ntiles;
         }
         if (bad) {
             sm.abort = 1;

@@ -100,6 +100,18 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
         : "r"(taddr));
 }
 #undef KPOOL_R8
+// tcgen05.wait::ld that also names the 32 registers of a pending tmem_ld32 as
+// read-write operands, so no use of them can be scheduled before the wait
+// when further loads are issued ahead of it.
+#define KPOOL_RW8(i) "+r"(r[i + 0]), "+r"(r[i + 1]), "+r"(r[i + 2]), "+r"(r[i + 3]), "+r"(r[i + 4]), \
+                     "+r"(r[i + 5]), "+r"(r[i + 6]), "+r"(r[i + 7])
+__device__ __forceinline__ void tmem_wait_ld32(uint32_t (&r)[32]) {
+    asm volatile("tcgen05.wait::ld.sync.aligned;\n"
+                 : KPOOL_RW8(0), KPOOL_RW8(8), KPOOL_RW8(16), KPOOL_RW8(24)
+                 :
+                 : "memory");
+}
+#undef KPOOL_RW8
 #define KPOOL_W8(i) "r"(r[i + 0]), "r"(r[i + 1]), "r"(r[i + 2]), "r"(r[i + 3]), "r"(r[i + 4]), "r"(r[i + 5]), \
                     "r"(r[i + 6]), "r"(r[i + 7])
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {

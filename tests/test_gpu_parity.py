@@ -40,7 +40,10 @@ def _check_kpool(res, inp, lay_o):
 
 
 def _full_parity(idx, rows=None, attn_rows=None):
-    wl = workloads.workload(idx)
+    return _parity_of(workloads.workload(idx), rows, attn_rows)
+
+
+def _parity_of(wl, rows=None, attn_rows=None, attention=True):
     inp = workloads.indexer_inputs(wl)
     dev = KP.to_dev(inp)
     res = KP.run_indexer(wl, dev)
@@ -80,6 +83,8 @@ def _full_parity(idx, rows=None, attn_rows=None):
           f"{stats['boundary_rows']} boundary rows ({stats['boundary_pools']} pools), hard {stats['hard']}; "
           f"score rel err {worst:.2e}")
     assert stats["hard"] == 0, stats["hard_rows"][:10]
+    if not attention:
+        return wl, res
 
     # attention, evaluated by the oracle on the GPU's own index rows
     attn_rows = rows if attn_rows is None else attn_rows
@@ -94,6 +99,14 @@ def _full_parity(idx, rows=None, attn_rows=None):
     print(f"[{wl.name}] attention: max abs {mx:.3e}, mean abs {mean:.3e}, lse {le:.3e}")
     assert mx <= KP.OUT_MAX_ABS and mean <= KP.OUT_MEAN_ABS and le <= KP.LSE_ABS
     return wl, res
+
+
+@pytest.mark.parametrize("hi", [4, 8, 16, 64])
+def test_tensor_core_scoring_head_counts(hi):
+    """The tcgen05 scoring kernel at every indexer head count it takes (d_i = 128): 256 / H_i queries per
+    work item, 1 to 8 queries per 32-column chunk; two documents, both long enough to have scored rows."""
+    wl = workloads.custom(f"heads{hi}", 20 + hi, (1637, 1130), n_idx_heads=hi, d_idx=128, topk=64, n_heads=4)
+    _parity_of(wl, attention=False)
 
 
 def test_parity_tiny_workload():
