@@ -74,6 +74,9 @@ def _peaks():
 # by the kernel generation it was taken on; another generation reports null
 # until it is captured.
 MLA_TRAFFIC_PER_TOKEN = {"mla-tc5": 537.2e6 / 4096, "mla-tc6": (309.190144e6 + 227.536640e6) / 4096}
+# DRAM bytes of one scoring launch (ncu dram__bytes_read.sum + dram__bytes_write.sum), captured at the
+# bench's own single-document T=32768 workload; tied to the kernel generation and used only for that T.
+SCORE_TRAFFIC_T32768 = {"score-tc2": 130.948352e6 + 474.102272e6}
 
 
 def _kernel_tags(K):
@@ -631,6 +634,11 @@ def main():
     for tag, per_tok in MLA_TRAFFIC_PER_TOKEN.items():
         if tag in tags:
             traffic = per_tok * wl.T          # scaled from the T=4096 capture (traffic grows with T)
+    score_traffic = None
+    if wl.T == 32768 and wl.doc_lens == (32768,):
+        for tag, b in SCORE_TRAFFIC_T32768.items():
+            if tag in tags:
+                score_traffic = b
     mla_tflops = work["mla_flops"] / (t["sparse_mla"] / 1e3) / 1e12
     score_tflops = work["score_flops"] / (t["score"] / 1e3) / 1e12
     fp8_peak = 2.0 * peaks["bf16_sustained"]
@@ -648,7 +656,7 @@ def main():
                      "peak_kind": f"bf16 sustained, {peaks['source']}",
                      "algorithmic": f"2*H*2D*valid_slots = {work['mla_flops']:.4e} FLOP per launch"},
         "indexer_roofline": {"bound": "tensor", "kernel": "score", "achieved": score_tflops, "peak": fp8_peak,
-                             "unit": "TFLOP/s", "frac": score_tflops / fp8_peak, "traffic": None,
+                             "unit": "TFLOP/s", "frac": score_tflops / fp8_peak, "traffic": score_traffic,
                              "peak_kind": "fp8 = 2 x bf16 sustained (nominal ratio)",
                              "algorithmic": f"2*H_i*d_i*pairs = {work['score_flops']:.4e} FLOP per launch"},
         "clocks": clk,
