@@ -44,7 +44,10 @@
 //              leaves lane l with slots 0-31 and lane l+16 with slots 32-63 of
 //              the summed row.  The running max only moves (and O^T is
 //              rescaled) when a slot beats it by more than 2^8; a vote on that
-//              is the only barrier of a block in the common case.  P^T goes to
+//              is the only barrier of a block in the common case.  When every
+//              slot of the warp's half-blocks is valid (all but a row's last
+//              block), the test runs on the unscaled block max and the scale is
+//              fused into the exponent's FMA.  P^T goes to
 //              shared memory in the operand layout; the epilogue writes O^T / l
 //              as bf16 straight from TMEM (lane pairs swap values so that every
 //              store covers two 64-byte runs of output rows).
@@ -471,11 +474,22 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
                     bad ? 0u
                         : (uint32_t)(*reinterpret_cast<volatile uint64_t*>(&sm.mask[s][0]) >> (32 * hs));
                 const float thr = m_ref + TAU;        // -inf for a row that has seen no valid slot yet
+                // every slot of the warp's half-blocks valid (all but a row's last block): x stays
+                // unscaled, the exceed test runs on the block max (scaling by a positive factor
+                // and rounding keep the order) and the scale is fused into the exponent's FMA
+                const bool full = __all_sync(0xffffffffu, mask == 0xffffffffu) && scale_log2 > 0.f;
                 bool exceed = false;
+                if (full) {
+                    float bm = x[0];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    x[j] = ((mask >> j) & 1u) ? x[j] * scale_log2 : -INFINITY;
-                    exceed |= x[j] > thr;
+                    for (int j = 1; j < 32; ++j) bm = fmaxf(bm, x[j]);
+                    exceed = bm * scale_log2 > thr;
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        x[j] = ((mask >> j) & 1u) ? x[j] * scale_log2 : -INFINITY;
+                        exceed |= x[j] > thr;
+                    }
                 }
                 // common case: no running max moves, one barrier per block
                 if (wg_or(bad || exceed)) {
@@ -483,6 +497,7 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
                     float bmax = -INFINITY;
 #pragma unroll
                     for (int j = 0; j < 32; ++j) bmax = fmaxf(bmax, x[j]);
+                    if (full) bmax *= scale_log2;
                     bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, 16));
                     float alpha = 1.f;
                     bool need = false;
@@ -521,16 +536,27 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
                 bad = bad || !warp_wait(tc::smem_u32(&sm.p_empty[sb]), ((g / NSB) & 1) ^ 1, abort_flag);
                 if (!bad) {
                     uint32_t pk[16];
-                    float ps = 0.f;
+                    float2 ps[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
                     const bool live = m_ref != -INFINITY;
+                    if (full) {
+                        const float nm = -m_ref;
 #pragma unroll
-                    for (int j = 0; j < 32; j += 2) {
-                        const float p0 = live ? fast_exp2(x[j] - m_ref) : 0.f;
-                        const float p1 = live ? fast_exp2(x[j + 1] - m_ref) : 0.f;
-                        ps += p0 + p1;
-                        pk[j >> 1] = pack_bf16(p0, p1);
+                        for (int j = 0; j < 32; j += 2) {
+                            const float2 p = make_float2(fast_exp2(fmaf(x[j], scale_log2, nm)),
+                                                         fast_exp2(fmaf(x[j + 1], scale_log2, nm)));
+                            ps[(j >> 1) & 1] = __fadd2_rn(ps[(j >> 1) & 1], p);
+                            pk[j >> 1] = pack_bf16(p.x, p.y);
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; j += 2) {
+                            const float2 p = make_float2(live ? fast_exp2(x[j] - m_ref) : 0.f,
+                                                         live ? fast_exp2(x[j + 1] - m_ref) : 0.f);
+                            ps[(j >> 1) & 1] = __fadd2_rn(ps[(j >> 1) & 1], p);
+                            pk[j >> 1] = pack_bf16(p.x, p.y);
+                        }
                     }
-                    l += ps;
+                    l += (ps[0].x + ps[1].x) + (ps[0].y + ps[1].y);
                     uint8_t* prow = smem + OFF_P + sb * P_BYTES;
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
