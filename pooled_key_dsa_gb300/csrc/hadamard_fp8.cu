@@ -8,7 +8,9 @@
 // the pair (x[j], x[j+h]) -> (x[j] + x[j+h], x[j] - x[j+h]), applied in
 // ascending stride order, then one multiply by fp32(1/sqrt(D)).  The scale is
 // amax/448 and the codes are E4M3(x * (448/amax)) with IEEE division and
-// round-to-nearest-even, saturating.
+// round-to-nearest-even, saturating.  A warp takes 4 consecutive vectors per
+// step, their loads issued together, and each cross-lane butterfly step is one
+// FMA by +-1 (the sum or difference rounded once, as before).
 #include <cstdint>
 #include <cuda_fp8.h>
 
@@ -18,6 +20,40 @@
 namespace kpool {
 
 template <int D, bool IN_BF16>
+__device__ __forceinline__ void load_vec(const void* __restrict__ x, int64_t v, bool valid, int lane, float (&e)[D / 32]) {
+    constexpr int E = D / 32;
+    if (!valid) {
+#pragma unroll
+        for (int j = 0; j < E; ++j) e[j] = 0.f;
+    } else if (IN_BF16) {
+        const uint16_t* src = static_cast<const uint16_t*>(x) + v * D + lane * E;
+        if (E == 4) {
+            const uint2 b = *reinterpret_cast<const uint2*>(src);
+            e[0] = __uint_as_float(b.x << 16);
+            e[1] = __uint_as_float(b.x & 0xffff0000u);
+            e[2 % E] = __uint_as_float(b.y << 16);
+            e[3 % E] = __uint_as_float(b.y & 0xffff0000u);
+        } else {
+            const uint32_t b = *reinterpret_cast<const uint32_t*>(src);
+            e[0] = __uint_as_float(b << 16);
+            e[1] = __uint_as_float(b & 0xffff0000u);
+        }
+    } else {
+        const float* src = static_cast<const float*>(x) + v * D + lane * E;
+        if (E == 4) {
+            const float4 f = *reinterpret_cast<const float4*>(src);
+            e[0] = f.x; e[1] = f.y; e[2 % E] = f.z; e[3 % E] = f.w;
+        } else {
+            const float2 f = *reinterpret_cast<const float2*>(src);
+            e[0] = f.x; e[1] = f.y;
+        }
+    }
+}
+
+// Each warp takes VPW consecutive vectors per step: their loads are issued together, so a warp
+// has VPW * 32 * E elements in flight instead of one vector's (the kernel is bound by memory-level
+// parallelism, not arithmetic); each vector's arithmetic is unchanged.
+template <int D, bool IN_BF16, int VPW>
 __global__ void __launch_bounds__(256) hadamard_fp8_kernel(const void* __restrict__ x, int64_t n_vec,
                                                            const int32_t* __restrict__ n_valid_dev,
                                                            const float* __restrict__ w,
@@ -28,90 +64,83 @@ __global__ void __launch_bounds__(256) hadamard_fp8_kernel(const void* __restric
     const int64_t warp0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
     const int64_t n_valid = n_valid_dev ? (int64_t)max(*n_valid_dev, 0) : n_vec;
-    for (int64_t v = warp0; v < n_vec; v += nwarps) {
-        float e[E];
-        if (v >= n_valid) {
+    for (int64_t v0 = warp0 * VPW; v0 < n_vec; v0 += nwarps * VPW) {
+        float e[VPW][E];
 #pragma unroll
-            for (int j = 0; j < E; ++j) e[j] = 0.f;
-        } else if (IN_BF16) {
-            const uint16_t* src = static_cast<const uint16_t*>(x) + v * D + lane * E;
-            if (E == 4) {
-                const uint2 b = *reinterpret_cast<const uint2*>(src);
-                e[0] = __uint_as_float(b.x << 16);
-                e[1] = __uint_as_float(b.x & 0xffff0000u);
-                e[2 % E] = __uint_as_float(b.y << 16);
-                e[3 % E] = __uint_as_float(b.y & 0xffff0000u);
-            } else {
-                const uint32_t b = *reinterpret_cast<const uint32_t*>(src);
-                e[0] = __uint_as_float(b << 16);
-                e[1] = __uint_as_float(b & 0xffff0000u);
-            }
-        } else {
-            const float* src = static_cast<const float*>(x) + v * D + lane * E;
-            if (E == 4) {
-                const float4 f = *reinterpret_cast<const float4*>(src);
-                e[0] = f.x; e[1] = f.y; e[2 % E] = f.z; e[3 % E] = f.w;
-            } else {
-                const float2 f = *reinterpret_cast<const float2*>(src);
-                e[0] = f.x; e[1] = f.y;
-            }
-        }
+        for (int u = 0; u < VPW; ++u) load_vec<D, IN_BF16>(x, v0 + u, v0 + u < n_valid && v0 + u < n_vec, lane, e[u]);
         // in-thread stages
 #pragma unroll
         for (int h = 1; h < E; h <<= 1) {
 #pragma unroll
-            for (int j = 0; j < E; ++j) {
-                if ((j & h) == 0) {
-                    const float a = e[j], b = e[j + h];
-                    e[j] = __fadd_rn(a, b);
-                    e[j + h] = __fsub_rn(a, b);
+            for (int u = 0; u < VPW; ++u)
+#pragma unroll
+                for (int j = 0; j < E; ++j) {
+                    if ((j & h) == 0) {
+                        const float a = e[u][j], b = e[u][j + h];
+                        e[u][j] = __fadd_rn(a, b);
+                        e[u][j + h] = __fsub_rn(a, b);
+                    }
                 }
-            }
         }
-        // cross-lane stages: the lane with the partner bit clear holds x[j]
+        // cross-lane stages: the lane with the partner bit clear holds x[j].  The pair's sum or
+        // difference is one FMA with a +-1 multiplier: fma(e, -1, other) rounds other - e once,
+        // exactly as the subtraction does (and fma(e, 1, other) rounds e + other).
 #pragma unroll
         for (int lb = 1; lb < 32; lb <<= 1) {
-            const bool high = (lane & lb) != 0;
+            const float sgn = (lane & lb) != 0 ? -1.f : 1.f;
+#pragma unroll
+            for (int u = 0; u < VPW; ++u)
+#pragma unroll
+                for (int j = 0; j < E; ++j) {
+                    const float other = __shfl_xor_sync(0xffffffffu, e[u][j], lb);
+                    e[u][j] = __fmaf_rn(e[u][j], sgn, other);
+                }
+        }
+        float amax[VPW];
+#pragma unroll
+        for (int u = 0; u < VPW; ++u) {
+            amax[u] = 0.f;
 #pragma unroll
             for (int j = 0; j < E; ++j) {
-                const float other = __shfl_xor_sync(0xffffffffu, e[j], lb);
-                e[j] = high ? __fsub_rn(other, e[j]) : __fadd_rn(e[j], other);
+                e[u][j] = __fmul_rn(e[u][j], c);
+                amax[u] = fmaxf(amax[u], fabsf(e[u][j]));
             }
         }
-        float amax = 0.f;
 #pragma unroll
-        for (int j = 0; j < E; ++j) {
-            e[j] = __fmul_rn(e[j], c);
-            amax = fmaxf(amax, fabsf(e[j]));
-        }
+        for (int o = 16; o > 0; o >>= 1)
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-        uint8_t q[E];
-        float s = 0.f;
-        if (amax > 0.f) {
-            const float inv = __fdiv_rn(448.f, amax);
-            s = __fdiv_rn(amax, 448.f);
+            for (int u = 0; u < VPW; ++u) amax[u] = fmaxf(amax[u], __shfl_xor_sync(0xffffffffu, amax[u], o));
 #pragma unroll
-            for (int j = 0; j < E; j += 2) {
-                const __nv_fp8x2_storage_t pr = __nv_cvt_float2_to_fp8x2(
-                    make_float2(__fmul_rn(e[j], inv), __fmul_rn(e[j + 1], inv)), __NV_SATFINITE, __NV_E4M3);
-                q[j] = (uint8_t)(pr & 0xff);
-                q[j + 1] = (uint8_t)(pr >> 8);
+        for (int u = 0; u < VPW; ++u) {
+            const int64_t v = v0 + u;
+            if (v >= n_vec) break;                      // warp-uniform
+            uint8_t q[E];
+            float s = 0.f;
+            if (amax[u] > 0.f) {
+                const float inv = __fdiv_rn(448.f, amax[u]);
+                s = __fdiv_rn(amax[u], 448.f);
+#pragma unroll
+                for (int j = 0; j < E; j += 2) {
+                    const __nv_fp8x2_storage_t pr = __nv_cvt_float2_to_fp8x2(
+                        make_float2(__fmul_rn(e[u][j], inv), __fmul_rn(e[u][j + 1], inv)), __NV_SATFINITE, __NV_E4M3);
+                    q[j] = (uint8_t)(pr & 0xff);
+                    q[j + 1] = (uint8_t)(pr >> 8);
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < E; ++j) q[j] = 0;
             }
-        } else {
-#pragma unroll
-            for (int j = 0; j < E; ++j) q[j] = 0;
-        }
-        uint8_t* dst = codes + v * D + lane * E;
-        if (E == 4) {
-            *reinterpret_cast<uint32_t*>(dst) =
-                (uint32_t)q[0] | ((uint32_t)q[1] << 8) | ((uint32_t)q[2 % E] << 16) | ((uint32_t)q[3 % E] << 24);
-        } else {
-            *reinterpret_cast<uint16_t*>(dst) = (uint16_t)((uint32_t)q[0] | ((uint32_t)q[1] << 8));
-        }
-        if (lane == 0) {
-            if (scales) scales[v] = s;
-            if (ws_out) ws_out[v] = w ? __fmul_rn(w[v], s) : s;
+            uint8_t* dst = codes + v * D + lane * E;
+            if (E == 4) {
+                *reinterpret_cast<uint32_t*>(dst) =
+                    (uint32_t)q[0] | ((uint32_t)q[1] << 8) | ((uint32_t)q[2 % E] << 16) | ((uint32_t)q[3 % E] << 24);
+            } else {
+                *reinterpret_cast<uint16_t*>(dst) = (uint16_t)((uint32_t)q[0] | ((uint32_t)q[1] << 8));
+            }
+            if (lane == 0) {
+                if (scales) scales[v] = s;
+                if (ws_out) ws_out[v] = w ? __fmul_rn(w[v], s) : s;
+            }
         }
     }
 }
@@ -120,18 +149,19 @@ int launch_hadamard_fp8(const void* x, bool in_bf16, int64_t n_vec, int d, const
                         const float* w, uint8_t* codes, float* scales, float* ws_out, cudaStream_t stream) {
     if (n_vec <= 0) return KPOOL_OK;
     const float c = (float)(1.0 / sqrt((double)d));
-    const int64_t want_blocks = (n_vec + 7) / 8;
+    constexpr int VPW = 4;
+    const int64_t want_blocks = (n_vec + 8 * VPW - 1) / (8 * VPW);
     const unsigned blocks = (unsigned)(want_blocks < 152 * 64 ? want_blocks : 152 * 64);
     if (d == 128) {
         if (in_bf16)
-            hadamard_fp8_kernel<128, true><<<blocks, 256, 0, stream>>>(x, n_vec, n_valid_dev, w, codes, scales, ws_out, c);
+            hadamard_fp8_kernel<128, true, VPW><<<blocks, 256, 0, stream>>>(x, n_vec, n_valid_dev, w, codes, scales, ws_out, c);
         else
-            hadamard_fp8_kernel<128, false><<<blocks, 256, 0, stream>>>(x, n_vec, n_valid_dev, w, codes, scales, ws_out, c);
+            hadamard_fp8_kernel<128, false, VPW><<<blocks, 256, 0, stream>>>(x, n_vec, n_valid_dev, w, codes, scales, ws_out, c);
     } else if (d == 64) {
         if (in_bf16)
-            hadamard_fp8_kernel<64, true><<<blocks, 256, 0, stream>>>(x, n_vec, n_valid_dev, w, codes, scales, ws_out, c);
+            hadamard_fp8_kernel<64, true, VPW><<<blocks, 256, 0, stream>>>(x, n_vec, n_valid_dev, w, codes, scales, ws_out, c);
         else
-            hadamard_fp8_kernel<64, false><<<blocks, 256, 0, stream>>>(x, n_vec, n_valid_dev, w, codes, scales, ws_out, c);
+            hadamard_fp8_kernel<64, false, VPW><<<blocks, 256, 0, stream>>>(x, n_vec, n_valid_dev, w, codes, scales, ws_out, c);
     } else {
         return KPOOL_ERR_SHAPE;
     }
