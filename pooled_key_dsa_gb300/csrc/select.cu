@@ -158,10 +158,18 @@ __device__ void select_registers(SelectSmem& s, const float* __restrict__ sc, in
     const uint32_t* tab = s.cand_key;
     uint32_t key[NC];
     uint32_t valid = 0;
+    // every load first, then the conversions: with sc in global memory (paged decode) the loads
+    // are then all in flight together instead of one round trip per key
+    float raw[NC];
 #pragma unroll
     for (int j = 0; j < NC; ++j) {
         const int p = SEL_THREADS * j + t;
-        key[j] = p < n ? score_key(sc[p]) : 0u;
+        raw[j] = p < n ? sc[p] : 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < NC; ++j) {
+        const int p = SEL_THREADS * j + t;
+        key[j] = p < n ? score_key(raw[j]) : 0u;
         valid |= (p < n ? 1u : 0u) << j;
     }
     // Radix levels over bits 31..21, 20..10, 9..0.  When the bin that holds the
