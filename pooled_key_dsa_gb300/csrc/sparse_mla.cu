@@ -49,7 +49,8 @@
 //              block), the test runs on the unscaled block max and the scale is
 //              fused into the exponent's FMA.  P^T goes to
 //              shared memory in the operand layout; the epilogue writes O^T / l
-//              as bf16 straight from TMEM (lane pairs swap values so that every
+//              as bf16 straight from TMEM, both 32-column halves of a tile
+//              loaded under one wait (lane pairs swap values so that every
 //              store covers two 64-byte runs of output rows).
 //   warps 8-9  S issuers (warp 8 also owns the TMEM allocation)
 //   warp 10    PV issuer
@@ -585,31 +586,27 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
             // instruction covers two 64-byte runs of the output rows.
             uint16_t* orow = out + (int64_t)i * H * D_LAT;
             const int odd = lane & 1;
+#pragma unroll 1
             for (int t = 0; t < 4; ++t) {
                 const int d = t * 128 + wid * 32 + (lane & ~1);
-#pragma unroll 1
-                for (int c0 = 0; c0 < HP; c0 += 32) {
-                    uint32_t o[32];
-                    if (nb > 0) {
-                        tc::tmem_ld32(tmem + lane_base + TM_O + 64 * t + c0, o);
-                        tc::tmem_wait_ld();
-                    } else {
+                // both 32-column halves of the tile in flight under one wait
+                uint32_t o[2][32];
+                if (nb > 0) {
+                    tc::tmem_ld32(tmem + lane_base + TM_O + 64 * t, o[0]);
+                    tc::tmem_ld32(tmem + lane_base + TM_O + 64 * t + 32, o[1]);
+                    tc::tmem_wait_ld();
+                } else {
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) o[j] = 0u;
-                    }
-                    float il[32];
+                    for (int j = 0; j < 32; ++j) o[0][j] = o[1][j] = 0u;
+                }
 #pragma unroll
-                    for (int j = 0; j < 32; j += 4) {
-                        const float4 q4 = *reinterpret_cast<const float4*>(&sm.inv_l[c0 + j]);
-                        il[j] = q4.x;
-                        il[j + 1] = q4.y;
-                        il[j + 2] = q4.z;
-                        il[j + 3] = q4.w;
-                    }
+                for (int hf = 0; hf < 2; ++hf) {
+                    const int c0 = 32 * hf;
 #pragma unroll
                     for (int j = 0; j < 32; j += 2) {
-                        const float a = __uint_as_float(o[j]) * il[j];
-                        const float b = __uint_as_float(o[j + 1]) * il[j + 1];
+                        const float2 il = *reinterpret_cast<const float2*>(&sm.inv_l[c0 + j]);
+                        const float a = __uint_as_float(o[hf][j]) * il.x;
+                        const float b = __uint_as_float(o[hf][j + 1]) * il.y;
                         const float recv = __shfl_xor_sync(0xffffffffu, odd ? a : b, 1);
                         const uint32_t w = odd ? pack_bf16(recv, b) : pack_bf16(a, recv);
                         const int hh = c0 + j + odd;
