@@ -257,6 +257,45 @@ def test_sparse_mla_index_range_and_empty_rows():
     assert mx <= KP.OUT_MAX_ABS and mean <= KP.OUT_MEAN_ABS and le <= KP.LSE_ABS
 
 
+def test_sparse_mla_holes_and_late_rescales():
+    """Rows mixing fully valid 64-slot blocks (the softmax's fast path) with blocks that have invalid
+    slots in the middle of the row (the masked path), and rows where a slot of a late full block
+    beats the running max by far, so that O^T is rescaled after several blocks have been added."""
+    wl = workloads.custom("mla_holes", 9, (700,), n_heads=64)
+    inp = workloads.indexer_inputs(wl)
+    ql = workloads.q_lat(wl)
+    kv = inp.kv_lat.float().clone()
+    T, W = wl.T, 640
+    rng = np.random.default_rng(3)
+    idx = np.full((T, W), -1, np.int32)
+    for i in range(T):
+        n = min(i + 1, W)
+        row = np.sort(rng.choice(i + 1, n, replace=False)).astype(np.int32)
+        if i % 3 == 1:                           # holes: about a fifth of the entries invalid
+            row[rng.random(n) < 0.2] = -1
+        idx[i, :n] = row
+    # late large logits: for every fourth long row, one slot of its sixth block gets the direction
+    # of one head's query, so that this head's logit there (~12) beats its running max by far while
+    # the key's entries stay of the usual size
+    big = []
+    for i in range(400, T, 4):
+        j = 5 * 64 + 7
+        if idx[i, j] >= 0 and int(idx[i, j]) not in big:
+            r = int(idx[i, j])
+            qh = ql[i, i % 64].float()
+            kv[r] = qh / qh.norm() * 12.0 / wl.scale / qh.norm()
+            big.append(r)
+    kv_b = kv.to(torch.bfloat16)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, lse = K.sparse_mla_fwd(ql.cuda(), kv_b.cuda(), torch.from_numpy(idx).cuda(), wl.scale, status=st)
+    assert K.check_status(st) == 0
+    rows = np.arange(T)
+    out_o, lse_o = O.sparse_attention(ql.float().numpy(), kv_b.float().numpy(), idx, wl.scale, rows)
+    mx, mean, le = KP.attention_check(out.float().cpu().numpy(), lse.cpu().numpy(), out_o, lse_o)
+    assert mx <= KP.OUT_MAX_ABS and mean <= KP.OUT_MEAN_ABS and le <= KP.LSE_ABS, (mx, mean, le)
+    assert len(big) > 10
+
+
 def test_small_head_counts_attention():
     for H in (1, 4, 20, 48):
         wl = workloads.custom("heads", 9, (97,), n_heads=H)
