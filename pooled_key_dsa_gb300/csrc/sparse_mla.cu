@@ -55,7 +55,9 @@
 //   warps 8-9  S issuers (warp 8 also owns the TMEM allocation)
 //   warp 10    PV issuer
 //   warp 11    row scanner: block count and range check of each query's
-//              index row, two queries ahead of the producers
+//              index row, two queries ahead of the producers (with one query
+//              per CTA, as in a decode step, nothing hides the scan: the
+//              ONE_QUERY instance reads the row with 16-byte loads)
 // Every wait is bounded and warp-uniform (lane 0 polls, the warp takes its
 // answer); on expiry the kernel records KPOOL_ERR_TIMEOUT, the softmax warps
 // agree on stopping at their next named barrier, every role leaves its loop,
@@ -159,6 +161,7 @@ __device__ __forceinline__ bool warp_wait(uint32_t addr, uint32_t parity, const 
 
 }  // namespace
 
+template <bool ONE_QUERY>
 __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_t* __restrict__ q_lat,
                                                                   const uint16_t* __restrict__ kv_lat,
                                                                   const int32_t* __restrict__ indices, int W,
@@ -411,12 +414,29 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
             const int32_t* irow = indices + (int64_t)i * W;
             int last = -1;
             bool out_of_range = false;
+            if (ONE_QUERY && (W & 3) == 0 && (reinterpret_cast<uintptr_t>(indices) & 15u) == 0) {
+                // one query per CTA (a decode step): no scan runs ahead of it, so the scan is
+                // exposed; 16-byte loads, eight in flight per lane
+                const int4* irow4 = reinterpret_cast<const int4*>(irow);
+#pragma unroll 8
+                for (int j4 = lane; j4 < (W >> 2); j4 += 32) {
+                    const int4 v4 = __ldg(irow4 + j4);
+                    const int vv[4] = {v4.x, v4.y, v4.z, v4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const bool valid = vv[e] >= 0 && vv[e] < T;
+                        last = valid ? 4 * j4 + e : last;
+                        out_of_range |= !valid && vv[e] != -1;
+                    }
+                }
+            } else {
 #pragma unroll 4
-            for (int j = lane; j < W; j += 32) {
-                const int v = __ldg(irow + j);
-                const bool valid = v >= 0 && v < T;
-                last = valid ? j : last;
-                out_of_range |= !valid && v != -1;
+                for (int j = lane; j < W; j += 32) {
+                    const int v = __ldg(irow + j);
+                    const bool valid = v >= 0 && v < T;
+                    last = valid ? j : last;
+                    out_of_range |= !valid && v != -1;
+                }
             }
             for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
             if (__any_sync(0xffffffffu, out_of_range) && lane == 0) set_status(status, KPOOL_ERR_INDEX_RANGE);
@@ -638,8 +658,10 @@ int launch_sparse_mla(const uint16_t* q_lat, const uint16_t* kv_lat, const int32
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return KPOOL_ERR_CUDA;
     if (n_sm[dev] == 0) {
-        if (cudaFuncSetAttribute(sparse_mla_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES) !=
-            cudaSuccess)
+        if (cudaFuncSetAttribute(sparse_mla_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 SMEM_BYTES) != cudaSuccess ||
+            cudaFuncSetAttribute(sparse_mla_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 SMEM_BYTES) != cudaSuccess)
             return KPOOL_ERR_CUDA;
         int sms = 0;
         if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return KPOOL_ERR_CUDA;
@@ -647,8 +669,12 @@ int launch_sparse_mla(const uint16_t* q_lat, const uint16_t* kv_lat, const int32
     }
     const int grid = n_rows < n_sm[dev] ? n_rows : n_sm[dev];
     const float scale_log2 = scale * 1.4426950408889634f;
-    sparse_mla_tc_kernel<<<grid, THREADS, SMEM_BYTES, stream>>>(q_lat, kv_lat, indices, W, n_rows, T, n_heads,
-                                                               scale_log2, out, lse, status);
+    if (n_rows <= n_sm[dev])                          // one query per CTA
+        sparse_mla_tc_kernel<true><<<grid, THREADS, SMEM_BYTES, stream>>>(q_lat, kv_lat, indices, W, n_rows, T,
+                                                                          n_heads, scale_log2, out, lse, status);
+    else
+        sparse_mla_tc_kernel<false><<<grid, THREADS, SMEM_BYTES, stream>>>(q_lat, kv_lat, indices, W, n_rows, T,
+                                                                           n_heads, scale_log2, out, lse, status);
     return cudaGetLastError() == cudaSuccess ? KPOOL_OK : KPOOL_ERR_CUDA;
 }
 
