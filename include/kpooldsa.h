@@ -363,6 +363,18 @@ int dsa_decode_index(const void* q_idx, const float* w, const uint8_t* k8_cache,
 int kpool_measure_l2_reduce(float* buf, int32_t rows, const int32_t* row_ids, int32_t n_ids,
                             kpool_stream_t stream);
 
+/* kpool_cast_e4m3: test and diagnostic utility, no counterpart on the pages.
+ * codes[k] = OCP E4M3 ("fn") code of x[k], k < n: round to nearest, ties to
+ * even, magnitudes above 448 saturate to 448, the sign follows the input.
+ * This is the conversion every FP8 quantiser of the library applies to its
+ * scaled values (prime-rl PR "GLM-5.3-Flash text model", Summary: queries and
+ * pooled keys are quantised to FP8), exposed so that it can be compared value
+ * by value with an independent encoder.
+ *   x      fp32 [n], device, 4-byte aligned
+ *   codes  uint8 [n], device
+ * Returns KPOOL_ERR_INVALID_ARG for null pointers with n > 0 or n < 0. */
+int kpool_cast_e4m3(const float* x, int64_t n, uint8_t* codes, kpool_stream_t stream);
+
 /* ----------------------------------------------------------------------
  * Absorbed-MLA projections either side of sparse_mla_fwd.
  * NeMo AutoModel PR "add GLM-5.3-Flash training support", Changelog: the K

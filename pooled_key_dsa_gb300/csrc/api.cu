@@ -160,6 +160,12 @@ int sparse_mla_bwd(const void* q_lat, const void* kv_lat, const int32_t* indices
                                  reinterpret_cast<cudaStream_t>(stream));
 }
 
+int kpool_cast_e4m3(const float* x, int64_t n, uint8_t* codes, kpool_stream_t stream) {
+    if (n < 0 || (n > 0 && (!x || !codes))) return KPOOL_ERR_INVALID_ARG;
+    if (!aligned(x, 4)) return KPOOL_ERR_ALIGN;
+    return launch_cast_e4m3(x, n, codes, reinterpret_cast<cudaStream_t>(stream));
+}
+
 int kpool_measure_l2_reduce(float* buf, int32_t rows, const int32_t* row_ids, int32_t n_ids,
                             kpool_stream_t stream) {
     if (rows < 0 || n_ids < 0) return KPOOL_ERR_SHAPE;

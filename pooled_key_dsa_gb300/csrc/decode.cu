@@ -110,10 +110,8 @@ __global__ void __launch_bounds__(128) paged_append_kernel(
             if (amax > 0.f) {
                 const float inv = __fdiv_rn(448.f, amax);
                 sc = __fdiv_rn(amax, 448.f);
-                const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(
-                    make_float2(__fmul_rn(e[0], inv), __fmul_rn(e[1], inv)), __NV_SATFINITE, __NV_E4M3);
-                const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(
-                    make_float2(__fmul_rn(e[2], inv), __fmul_rn(e[3], inv)), __NV_SATFINITE, __NV_E4M3);
+                const uint16_t lo = cvt_e4m3x2(__fmul_rn(e[0], inv), __fmul_rn(e[1], inv));
+                const uint16_t hi = cvt_e4m3x2(__fmul_rn(e[2], inv), __fmul_rn(e[3], inv));
                 packed = (uint32_t)lo | ((uint32_t)hi << 16);
             }
             const int64_t slot = (int64_t)page * PAGE_POOLS + (pidx % PAGE_POOLS);

@@ -121,8 +121,7 @@ __global__ void __launch_bounds__(256) hadamard_fp8_kernel(const void* __restric
                 s = __fdiv_rn(amax[u], 448.f);
 #pragma unroll
                 for (int j = 0; j < E; j += 2) {
-                    const __nv_fp8x2_storage_t pr = __nv_cvt_float2_to_fp8x2(
-                        make_float2(__fmul_rn(e[u][j], inv), __fmul_rn(e[u][j + 1], inv)), __NV_SATFINITE, __NV_E4M3);
+                    const uint16_t pr = cvt_e4m3x2(__fmul_rn(e[u][j], inv), __fmul_rn(e[u][j + 1], inv));
                     q[j] = (uint8_t)(pr & 0xff);
                     q[j + 1] = (uint8_t)(pr >> 8);
                 }
@@ -143,6 +142,30 @@ __global__ void __launch_bounds__(256) hadamard_fp8_kernel(const void* __restric
             }
         }
     }
+}
+
+// E4M3 codes of n fp32 values with the quantisers' conversion (a test and
+// diagnostic entry: the oracle's encoder is checked against it value by value).
+__global__ void __launch_bounds__(256) cast_e4m3_kernel(const float* __restrict__ x, int64_t n,
+                                                        uint8_t* __restrict__ codes) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x * 2;
+    for (int64_t i = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 2; i < n; i += stride) {
+        if (i + 1 < n) {
+            const uint16_t c = cvt_e4m3x2(x[i], x[i + 1]);
+            codes[i] = (uint8_t)(c & 0xff);
+            codes[i + 1] = (uint8_t)(c >> 8);
+        } else {
+            codes[i] = (uint8_t)(cvt_e4m3x2(x[i], 0.f) & 0xff);
+        }
+    }
+}
+
+int launch_cast_e4m3(const float* x, int64_t n, uint8_t* codes, cudaStream_t stream) {
+    if (n <= 0) return KPOOL_OK;
+    const int64_t want = (n + 511) / 512;
+    const unsigned blocks = (unsigned)(want < 152 * 32 ? want : 152 * 32);
+    cast_e4m3_kernel<<<blocks, 256, 0, stream>>>(x, n, codes);
+    return cudaGetLastError() == cudaSuccess ? KPOOL_OK : KPOOL_ERR_CUDA;
 }
 
 int launch_hadamard_fp8(const void* x, bool in_bf16, int64_t n_vec, int d, const int32_t* n_valid_dev,

@@ -3,6 +3,7 @@
 
 #include <cstdint>
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include "kpooldsa.h"
@@ -40,5 +41,12 @@ __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
 }
 
 __host__ __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// E4M3 codes of two fp32 values (round to nearest, ties to even; magnitudes
+// above 448 saturate to 448), low byte from `lo`: the one conversion every
+// FP8 quantiser of the library uses (and kpool_cast_e4m3 exposes for tests).
+__device__ __forceinline__ uint16_t cvt_e4m3x2(float lo, float hi) {
+    return (uint16_t)__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
+}
 
 }  // namespace kpool

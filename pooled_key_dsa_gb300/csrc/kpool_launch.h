@@ -22,6 +22,7 @@ int launch_kpool_build(const void* k, const float* gate, const float* ape, const
 // in_bf16 selects the input type (bf16 queries or fp32 pooled keys).  If
 // n_valid_dev is non-null, vectors at or past *n_valid_dev get zero codes and
 // scale.  If w is non-null, ws_out[v] = w[v] * scale[v]; scales may be null.
+int launch_cast_e4m3(const float* x, int64_t n, uint8_t* codes, cudaStream_t stream);
 int launch_hadamard_fp8(const void* x, bool in_bf16, int64_t n_vec, int d, const int32_t* n_valid_dev,
                         const float* w, uint8_t* codes, float* scales, float* ws_out, cudaStream_t stream);
 

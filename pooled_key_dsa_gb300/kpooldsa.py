@@ -24,7 +24,7 @@ EXPORTED = ("kpool_workspace_bytes", "kpool_workspace_offsets", "kpool_build", "
             "kpool_stage_select", "kpool_set_stage_events", "kpool_check_status", "kpool_strerror", "kpool_version",
             "dsa_index_noalloc", "sparse_mla_fwd_rows", "kpool_forward_host", "mla_absorb_q", "mla_v_proj",
             "sparse_mla_bwd", "kpool_measure_l2_reduce", "kpool_paged_append", "dsa_decode_workspace_bytes",
-            "dsa_decode_index")
+            "dsa_decode_index", "kpool_cast_e4m3")
 
 
 class KpoolUnavailable(ImportError):
@@ -91,6 +91,7 @@ def lib():
                                          ctypes.POINTER(Params), i32, vp, vp, vp]
         L.sparse_mla_bwd.argtypes = [vp, vp, vp, i32, i32, i32, ctypes.c_float, vp, vp, vp, vp, vp, vp, vp, vp]
         L.kpool_measure_l2_reduce.argtypes = [vp, i32, vp, i32, vp]
+        L.kpool_cast_e4m3.argtypes = [vp, ctypes.c_int64, vp, vp]
         L.kpool_paged_append.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, ctypes.POINTER(Params), vp, vp,
                                          vp, vp]
         L.dsa_decode_workspace_bytes.argtypes = [ctypes.POINTER(Params), i32, i32]
@@ -314,6 +315,18 @@ def measure_l2_reduce(buf, row_ids, stream=None):
         raise ValueError("buf must be [rows, 512]")
     _check(lib().kpool_measure_l2_reduce(_ptr(buf), buf.shape[0], _ptr(row_ids), row_ids.numel(), _stream(stream)),
            "kpool_measure_l2_reduce")
+
+
+def cast_e4m3(x, out=None, stream=None):
+    """uint8 E4M3 codes of the fp32 tensor x (round to nearest even, saturating at 448): the conversion that
+    every FP8 quantiser of the library applies, exposed for value-by-value tests."""
+    _want(x, torch.float32, None, "x")
+    if not x.is_contiguous():
+        raise ValueError("x must be contiguous")
+    if out is None:
+        out = torch.empty(x.shape, dtype=torch.uint8, device=x.device)
+    _check(lib().kpool_cast_e4m3(_ptr(x), x.numel(), _ptr(out), _stream(stream)), "kpool_cast_e4m3")
+    return out
 
 
 # ----------------------------------------------------------------- paged decode

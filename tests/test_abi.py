@@ -128,6 +128,16 @@ def test_host_checks_of_the_projection_entries(lib):
         assert fn(None, None, 0, 64, 128, 128, None, None, None) == K.KPOOL_OK        # T = 0: nothing to do
 
 
+def test_host_checks_of_the_cast_entry(lib):
+    vp = ctypes.c_void_p
+    cast = lib.kpool_cast_e4m3
+    assert cast(vp(16), -1, vp(16), None) == K.CODES["KPOOL_ERR_INVALID_ARG"]
+    assert cast(None, 8, vp(16), None) == K.CODES["KPOOL_ERR_INVALID_ARG"]
+    assert cast(vp(16), 8, None, None) == K.CODES["KPOOL_ERR_INVALID_ARG"]
+    assert cast(vp(18), 8, vp(16), None) == K.CODES["KPOOL_ERR_ALIGN"]
+    assert cast(None, 0, None, None) == K.KPOOL_OK          # nothing to convert
+
+
 def test_host_checks_of_the_backward_entry(lib):
     vp = ctypes.c_void_p
     ok = [vp(16)] * 3
