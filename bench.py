@@ -110,6 +110,29 @@ def _work(wl):
     }
 
 
+def layer_roofline(wl, work, t, peaks, fp8_peak):
+    """The end-to-end layer's fraction of roofline: sum over the step's stages of the roofline time (each stage's
+    algorithmic FLOPs or bytes over the measured peak it is bound by) divided by the sum of the measured stage
+    times.  Bytes per stage: pooling reads k (2 d_i B) and gate (4 d_i B) per token and writes d_i B per token of
+    pooled keys; Hadamard/FP8 reads 2 d_i B and writes d_i B of codes plus a scale and a head weight per (token,
+    indexer head), and the same for the pooled keys (4 d_i B in); select writes the index rows (the scores it
+    reads are the scoring's materialised output, counted as design overhead, not as algorithmic bytes); the
+    sparse MLA is max(its FLOPs on the bf16 peak, q_lat + out + kv_lat + rows + lse over HBM)."""
+    hbm = peaks["hbm_gbs"] * 1e9
+    T, di, Hi = wl.T, wl.d_idx, wl.n_idx_heads
+    roof = {
+        "kpool_build": (7.0 * di * T) / hbm * 1e3,
+        "hadamard_fp8": (T * Hi * (3.0 * di + 8) + (T // 4) * (5.0 * di + 4)) / hbm * 1e3,
+        "score": work["score_flops"] / (fp8_peak * 1e12) * 1e3,
+        "select": (4.0 * T * wl.W) / hbm * 1e3,
+        "sparse_mla": max(work["mla_flops"] / (peaks["bf16_sustained"] * 1e12), work["mla_hbm_bytes"] / hbm) * 1e3,
+    }
+    meas = {k: t[k] for k in roof}
+    return {"frac": sum(roof.values()) / sum(meas.values()), "t_roof_ms": roof, "t_ms": meas,
+            "peaks": {"hbm_GBs": peaks["hbm_gbs"], "bf16_TFLOPs": peaks["bf16_sustained"], "fp8_TFLOPs": fp8_peak,
+                      "source": peaks["source"]}}
+
+
 # ----------------------------------------------------------------- ranks
 
 def max_over_ranks(value: float, world: int, device) -> float:
@@ -645,6 +668,7 @@ def main():
     mla_tflops = work["mla_flops"] / (t["sparse_mla"] / 1e3) / 1e12
     score_tflops = work["score_flops"] / (t["score"] / 1e3) / 1e12
     fp8_peak = 2.0 * peaks["bf16_sustained"]
+    layer = layer_roofline(wl, work, t, peaks, fp8_peak)
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": a.steps,
         "warmup": a.warmup, "ms_per_step": total_ms / a.steps, "higher_is_better": True, "scaling": "weak",
@@ -662,6 +686,7 @@ def main():
                              "unit": "TFLOP/s", "frac": score_tflops / fp8_peak, "traffic": score_traffic,
                              "peak_kind": "fp8 = 2 x bf16 sustained (nominal ratio)",
                              "algorithmic": f"2*H_i*d_i*pairs = {work['score_flops']:.4e} FLOP per launch"},
+        "layer_roofline": layer,
         "clocks": clk,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "api": f"kpool_forward_host, {a.chunks} query-row blocks, page-locked host buffers"},

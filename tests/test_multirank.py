@@ -69,3 +69,22 @@ def test_reference_arm_prints_on_rank_zero_only():
     line = json.loads(r0.stdout.strip().splitlines()[-1])
     assert line["impl"] == "reference" and line["value"] > 0 and line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["n_gpus"] == 2
+
+
+def test_layer_roofline_fraction_of_the_step():
+    """The layer's fraction of roofline is the sum of the stages' roofline times over the sum of their measured
+    times; stages measured at their roofline give 1, and the headline workload's roofline time is the sparse
+    MLA's bf16 FLOPs plus the scoring's FP8 FLOPs plus three HBM-bound stages."""
+    from pooled_key_dsa_gb300 import workloads
+    wl = workloads.workload(3)
+    work = bench._work(wl)
+    peaks = {"hbm_gbs": 6000.0, "bf16_sustained": 1700.0, "source": "test"}
+    first = bench.layer_roofline(wl, work, {k: 1.0 for k in ("kpool_build", "hadamard_fp8", "score", "select",
+                                                              "sparse_mla")}, peaks, 3400.0)
+    r = first["t_roof_ms"]
+    assert abs(r["sparse_mla"] - work["mla_flops"] / 1700e12 * 1e3) < 1e-12
+    assert abs(r["score"] - work["score_flops"] / 3400e12 * 1e3) < 1e-12
+    assert abs(r["select"] - 4.0 * wl.T * wl.W / 6000e9 * 1e3) < 1e-12
+    at_roof = bench.layer_roofline(wl, work, dict(r), peaks, 3400.0)
+    assert abs(at_roof["frac"] - 1.0) < 1e-12
+    assert abs(first["frac"] - sum(r.values()) / 5.0) < 1e-12
