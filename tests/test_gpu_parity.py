@@ -296,6 +296,29 @@ def test_sparse_mla_holes_and_late_rescales():
     assert len(big) > 10
 
 
+@pytest.mark.parametrize("H, W", [(48, 130), (16, 256), (64, 2176)])
+def test_one_query_per_cta_launches(H, W):
+    """Launches with at most one query per CTA (as a decode step makes) take the kernel's one-query instance,
+    whose row scanner reads the row with 16-byte loads when W is a multiple of 4 and 4-byte loads otherwise."""
+    T, n_rows = 3000, 40
+    rng = np.random.default_rng(H + W)
+    q = torch.from_numpy(rng.standard_normal((n_rows, H, 512), dtype=np.float32)).to(torch.bfloat16)
+    kv = torch.from_numpy(rng.standard_normal((T, 512), dtype=np.float32)).to(torch.bfloat16)
+    idx = np.full((n_rows, W), -1, np.int32)
+    for i in range(n_rows):
+        n = int(rng.integers(0, W + 1))
+        idx[i, :n] = rng.choice(T, n, replace=False)
+    idx[3, :] = -1                               # an empty row
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, lse = K.sparse_mla_fwd_rows(q.cuda(), kv.cuda(), torch.from_numpy(idx).cuda(), 1.0 / np.sqrt(512),
+                                     status=st)
+    assert K.check_status(st) == 0
+    out_o, lse_o = O.sparse_attention(q.float().numpy(), kv.float().numpy(), idx, 1.0 / np.sqrt(512),
+                                      np.arange(n_rows))
+    mx, mean, le = KP.attention_check(out.float().cpu().numpy(), lse.cpu().numpy(), out_o, lse_o)
+    assert mx <= KP.OUT_MAX_ABS and mean <= KP.OUT_MEAN_ABS and le <= KP.LSE_ABS, (mx, mean, le)
+
+
 def test_small_head_counts_attention():
     for H in (1, 4, 20, 48):
         wl = workloads.custom("heads", 9, (97,), n_heads=H)
