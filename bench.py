@@ -44,7 +44,7 @@ def _args():
     ap.add_argument("--config", type=int, default=3, help="workload index (3 = T=32768 headline)")
     ap.add_argument("--cpu-rows", type=int, default=4096, help="query rows in the CPU-oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--chunks", type=int, default=8, help="query-row blocks of the end-to-end pipeline")
+    ap.add_argument("--chunks", type=int, default=16, help="query-row blocks of the end-to-end pipeline")
     ap.add_argument("--only-index", action="store_true",
                     help="profiling aid: run kpool_build + dsa_index only (no q_lat / out allocation)")
     ap.add_argument("--only-proj", action="store_true",
