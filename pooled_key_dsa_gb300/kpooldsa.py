@@ -412,7 +412,7 @@ def mla_v_proj(o_lat, w_kv_b, d_nope: int, d_v: int, out=None, status=None, stre
 _HOST_KEYS = ("k", "gate", "ape", "cu_seqlens", "q_idx", "w", "q_lat", "kv_lat", "out", "lse")
 
 
-def forward_host(host: dict, dev: dict, layout: PoolLayout, p: Params, n_chunks: int = 8, streams=None):
+def forward_host(host: dict, dev: dict, layout: PoolLayout, p: Params, n_chunks: int = 16, streams=None):
     """Whole forward from (page-locked) host tensors with overlapped copies.
 
     host: CPU tensors k, gate, ape, cu_seqlens, q_idx, w, q_lat, kv_lat (read) and out, lse (written).
