@@ -129,15 +129,34 @@ __global__ void kpool_pool_kernel(const uint16_t* __restrict__ k, const float* _
 #pragma unroll
     for (int ch = 0; ch < 4; ++ch) {
         double m = lg[0][ch];
+        int jm = 0;                                   // first index holding the max: its weight is exp(0) = 1
 #pragma unroll
-        for (int j = 1; j < KPOOL; ++j) m = fmax(m, lg[j][ch]);
+        for (int j = 1; j < KPOOL; ++j) {
+            jm = lg[j][ch] > m ? j : jm;
+            m = fmax(m, lg[j][ch]);
+        }
+        // exp of the other three logits only (gathered so that every lane runs the same three exps)
+        double o[KPOOL - 1];
+#pragma unroll
+        for (int k = 0; k < KPOOL - 1; ++k) {
+            const int j = k + (k >= jm ? 1 : 0);
+            double v = lg[0][ch];
+#pragma unroll
+            for (int jj = 1; jj < KPOOL; ++jj) v = j == jj ? lg[jj][ch] : v;
+            o[k] = exp(__dsub_rn(v, m));
+        }
         double e[KPOOL];
-        double s = 0.0;
 #pragma unroll
         for (int j = 0; j < KPOOL; ++j) {
-            e[j] = exp(__dsub_rn(lg[j][ch], m));
-            s = __dadd_rn(s, e[j]);
+            const int k = j < jm ? j : j - 1;
+            double v = 1.0;
+#pragma unroll
+            for (int kk = 0; kk < KPOOL - 1; ++kk) v = (j != jm && k == kk) ? o[kk] : v;
+            e[j] = v;
         }
+        double s = 0.0;
+#pragma unroll
+        for (int j = 0; j < KPOOL; ++j) s = __dadd_rn(s, e[j]);
         double acc = 0.0;
 #pragma unroll
         for (int j = 0; j < KPOOL; ++j) acc = __dadd_rn(acc, __dmul_rn(__ddiv_rn(e[j], s), kv[j][ch]));
