@@ -319,6 +319,27 @@ def test_one_query_per_cta_launches(H, W):
     assert mx <= KP.OUT_MAX_ABS and mean <= KP.OUT_MEAN_ABS and le <= KP.LSE_ABS, (mx, mean, le)
 
 
+@pytest.mark.parametrize("hi, di", [(32, 128), (4, 64)])
+def test_indexer_queries_only_8_byte_aligned(hi, di):
+    """q_idx is documented as 8-byte aligned: a view starting 8 bytes into an allocation (so not 16-byte
+    aligned) gives the same codes, head weights and index rows as an aligned copy."""
+    wl = workloads.custom("qalign", 17, (700, 333), n_idx_heads=hi, d_idx=di, topk=32, n_heads=4)
+    inp = workloads.indexer_inputs(wl)
+    dev = KP.to_dev(inp)
+    ref = KP.run_indexer(wl, dev)
+    n = dev["q_idx"].numel()
+    buf = torch.empty(n + 4, dtype=torch.bfloat16, device="cuda")
+    buf[4:] = dev["q_idx"].reshape(-1)
+    shifted = buf[4:].view(dev["q_idx"].shape)
+    assert shifted.data_ptr() % 16 == 8
+    dev2 = dict(dev, q_idx=shifted)
+    got = KP.run_indexer(wl, dev2)
+    assert got["status"] == 0
+    np.testing.assert_array_equal(got["q8"], ref["q8"])
+    np.testing.assert_array_equal(got["ws"].view(np.uint32), ref["ws"].view(np.uint32))
+    np.testing.assert_array_equal(got["indices"], ref["indices"])
+
+
 def test_small_head_counts_attention():
     for H in (1, 4, 20, 48):
         wl = workloads.custom("heads", 9, (97,), n_heads=H)
