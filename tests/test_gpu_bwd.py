@@ -159,7 +159,10 @@ def test_backward_empty_rows_out_of_range_and_repeatability():
     assert K.check_status(st) == K.CODES["KPOOL_ERR_INDEX_RANGE"]
     dq2, dkv2 = K.sparse_mla_bwd(qd, kvd, idd, wl.scale, out, lse, dd)
     assert torch.equal(dq, dq2)                                      # dq has a fixed summation order
-    assert torch.allclose(dkv, dkv2, rtol=1e-5, atol=1e-6)           # dkv: atomics, order may vary
+    # dkv: fp32 atomics whose order varies between runs.  An element sums up to ~1000 contributions, so two
+    # runs differ by the rounding of two summation orders (a few 1e-6 absolute at this magnitude), which a
+    # fixed 1e-6 floor does not cover near zero; the floor is set by the tensor's own scale instead.
+    assert torch.allclose(dkv, dkv2, rtol=1e-5, atol=2e-5 * float(dkv.abs().max()))
     ref_idx = idx.copy()
     ref_idx[(ref_idx < -1) | (ref_idx >= wl.T)] = -1
     ref = O.sparse_attention_bwd(q.float().numpy(), kv.float().numpy(), ref_idx, wl.scale, dout.float().numpy(),
