@@ -12,16 +12,18 @@
 // 20..10, 9..0) over the registers finds the key K of the topk-th best pool
 // and how many pools equal to K still fit, and the ordered compaction ranks
 // the kept pools with one ballot per 256-pool column and one block scan over
-// the (column, warp) counts.  Longer rows take the streaming path below.
+// the (column, warp) counts.  The kept pools are those with key > K plus the
+// first pools with key == K that still fit (lower pool index wins ties); their
+// positions are written in pool order, so the row comes out ascending without
+// a sort.
 //
-// Streaming path: a three-level radix select (bits 31..20, 19..8, 7..0) finds the key K
-// of the topk-th best pool and how many pools equal to K still fit
-// (`need_eq`).  Level 1 histograms every key; the pools in the chosen level-1
-// bin are copied to a shared candidate list that levels 2 and 3 refine (if the
-// list overflows, those levels re-read the row).  A final ordered pass keeps
-// the pools with key > K plus the first `need_eq` pools with key == K (lower
-// pool index wins ties) and writes their positions in pool order, so the row
-// comes out ascending without a sort.
+// Longer rows (documents of more than 32768 tokens) are ranked in chunks of
+// 8192 pools: the same levels, and the same compaction chunk by chunk,
+// carrying the kept and tied counts from one chunk to the next.  A row of up
+// to 16392 pools is first copied whole into shared memory; a longer one is
+// read from global memory on every pass, and a pass after level 1 copies the
+// keys of the chosen level-1 bin to a shared candidate list that levels 2 and
+// 3 then run over.
 #include <cstdint>
 
 #include "kpool_common.cuh"
@@ -33,12 +35,13 @@ namespace {
 
 constexpr int SEL_THREADS = 256;
 constexpr int SEL_WARPS = SEL_THREADS / 32;
-constexpr int HIST_BINS = 4096;
-constexpr int CAND_CAP = 4096;
+constexpr int HIST_BINS = 2048;
+constexpr int DECODE_CAND_CAP = 4096;                 // candidate list of the decode select's long rows
 
+// hist also serves as the (column, warp) rank table of the ordered compaction once the radix
+// levels are done.
 struct SelectSmem {
     uint32_t hist[HIST_BINS];
-    uint32_t cand_key[CAND_CAP];
     int32_t warp_tot[SEL_WARPS];
     uint32_t n_cand;
     uint32_t digit;
@@ -131,23 +134,25 @@ __device__ __forceinline__ void fast_level(SelectSmem& s, const uint32_t (&key)[
 }
 
 // Ranks, in pool order, of per-thread flags held as one bit per column: afterwards pool
-// 256j + t has rank tab[8j + warp] + popc(bal[j] & lanes below).  tab (256 entries, one per
-// (column, warp) in that order) holds the exclusive scan of the per-(column, warp) counts.
-// The caller reads tab, then synchronises before tab is reused.
+// 256j + t has rank tab[8j + warp] + popc(ballot of column j & lanes below).  tab (256 entries,
+// one per (column, warp) in that order, in s.hist) holds the exclusive scan of the
+// per-(column, warp) counts.  The caller reads tab, then synchronises before tab is reused.
+// Returns the number of flags set.
 template <int NC>
-__device__ __forceinline__ void column_scan(SelectSmem& s, uint32_t flags, uint32_t (&bal)[NC]) {
+__device__ __forceinline__ int column_scan(SelectSmem& s, uint32_t flags) {
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
-    uint32_t* tab = s.cand_key;                      // free on this path
+    uint32_t* tab = s.hist;                          // the radix levels are done with it
 #pragma unroll
     for (int j = 0; j < NC; ++j) {
-        bal[j] = __ballot_sync(0xffffffffu, (flags >> j) & 1u);
-        if (lane == 0) tab[8 * j + wid] = __popc(bal[j]);
+        const uint32_t b = __ballot_sync(0xffffffffu, (flags >> j) & 1u);
+        if (lane == 0) tab[8 * j + wid] = __popc(b);
     }
     __syncthreads();
     int total;
     const int before = block_excl_scan(threadIdx.x < 8 * NC ? (int)tab[threadIdx.x] : 0, s.warp_tot, total);
     tab[threadIdx.x] = (uint32_t)before;
     __syncthreads();
+    return total;
 }
 
 template <int NC, typename Map>
@@ -155,7 +160,7 @@ __device__ void select_registers(SelectSmem& s, const float* __restrict__ sc, in
                                  int32_t* __restrict__ row) {
     const int t = threadIdx.x, wid = t >> 5;
     const uint32_t below = (1u << (t & 31)) - 1u;
-    const uint32_t* tab = s.cand_key;
+    const uint32_t* tab = s.hist;
     uint32_t key[NC];
     uint32_t valid = 0;
     // every load first, then the conversions: with sc in global memory (paged decode) the loads
@@ -205,18 +210,21 @@ __device__ void select_registers(SelectSmem& s, const float* __restrict__ sc, in
         eq |= (v && !whole && key[j] == K ? 1u : 0u) << j;
     }
     uint32_t take = gt | eq;
-    uint32_t bal[NC];
+    // the column ballots are taken again where the ranks are read: keeping them costs NC registers
     if (n_eq != need_eq) {                           // ties at K: the lowest pool indices among them win
-        column_scan(s, eq, bal);
+        column_scan<NC>(s, eq);
 #pragma unroll
-        for (int j = 0; j < NC; ++j)
-            if (((eq >> j) & 1u) && tab[8 * j + wid] + __popc(bal[j] & below) >= need_eq) take &= ~(1u << j);
+        for (int j = 0; j < NC; ++j) {
+            const uint32_t b = __ballot_sync(0xffffffffu, (eq >> j) & 1u);
+            if (((eq >> j) & 1u) && tab[8 * j + wid] + __popc(b & below) >= need_eq) take &= ~(1u << j);
+        }
         __syncthreads();
     }
-    column_scan(s, take, bal);
+    column_scan<NC>(s, take);
 #pragma unroll
     for (int j = 0; j < NC; ++j) {
-        const uint32_t rank = tab[8 * j + wid] + __popc(bal[j] & below);
+        const uint32_t b = __ballot_sync(0xffffffffu, (take >> j) & 1u);
+        const uint32_t rank = tab[8 * j + wid] + __popc(b & below);
         if (((take >> j) & 1u) && rank < (uint32_t)topk) {
             const int pos = map.pool(SEL_THREADS * j + t);
             *reinterpret_cast<int4*>(row + KPOOL * rank) = make_int4(pos, pos + 1, pos + 2, pos + 3);
@@ -226,90 +234,149 @@ __device__ void select_registers(SelectSmem& s, const float* __restrict__ sc, in
 
 }  // namespace
 
-// Streaming path for rows of more than FAST_MAX candidate pools: the row is
-// read from global memory on every pass.  r is the query's position in its
-// document or sequence.
+// Keys of chunk c0 (pools c0 + 256j + t in key j) of a row in global memory.
+__device__ __forceinline__ void load_chunk(const float* __restrict__ sc, int n, int c0, uint32_t (&key)[FAST_KPT],
+                                           uint32_t& valid) {
+    float raw[FAST_KPT];
+#pragma unroll
+    for (int j = 0; j < FAST_KPT; ++j) {
+        const int p = c0 + SEL_THREADS * j + (int)threadIdx.x;
+        raw[j] = p < n ? sc[p] : 0.f;
+    }
+    valid = 0;
+#pragma unroll
+    for (int j = 0; j < FAST_KPT; ++j) {
+        const int p = c0 + SEL_THREADS * j + (int)threadIdx.x;
+        key[j] = p < n ? score_key(raw[j]) : 0u;
+        valid |= (p < n ? 1u : 0u) << j;
+    }
+}
+
+// One radix level over every chunk of a long row (see fast_level).
+__device__ __forceinline__ void chunk_level(SelectSmem& s, const float* __restrict__ sc, int n, uint32_t hi_mask, uint32_t prefix,
+                            int shift, int nbins, uint32_t remaining) {
+    for (int b = threadIdx.x; b < nbins; b += SEL_THREADS) s.hist[b] = 0;
+    __syncthreads();
+    for (int c0 = 0; c0 < n; c0 += FAST_MAX) {
+        uint32_t key[FAST_KPT], valid;
+        load_chunk(sc, n, c0, key, valid);
+#pragma unroll
+        for (int j = 0; j < FAST_KPT; ++j)
+            if (((valid >> j) & 1u) && (key[j] & hi_mask) == prefix)
+                atomicAdd(&s.hist[(key[j] >> shift) & (uint32_t)(nbins - 1)], 1u);
+    }
+    __syncthreads();
+    pick_digit(s, nbins, remaining);
+}
+
+// One radix level over the candidate list (the keys of the chosen level-1 bin).
+__device__ __forceinline__ void list_level(SelectSmem& s, const uint32_t* cand, uint32_t n_list, uint32_t hi_mask,
+                                           uint32_t prefix, int shift, int nbins, uint32_t remaining) {
+    for (int b = threadIdx.x; b < nbins; b += SEL_THREADS) s.hist[b] = 0;
+    __syncthreads();
+    for (uint32_t c = threadIdx.x; c < n_list; c += SEL_THREADS) {
+        const uint32_t key = cand[c];
+        if ((key & hi_mask) == prefix) atomicAdd(&s.hist[(key >> shift) & (uint32_t)(nbins - 1)], 1u);
+    }
+    __syncthreads();
+    pick_digit(s, nbins, remaining);
+}
+
+// Rows of more than FAST_MAX candidate pools: the register path's levels and compaction, chunk by
+// chunk; sc is in global or shared memory.  After level 1 the keys of the chosen bin are copied to
+// `cand` (cand_cap keys; when the bin holds more, or cand is null, levels 2 and 3 re-read the row
+// instead).  The compaction walks the chunks in pool order
+// with the running count of kept pools (the rank base) and of pools tied at K (which decides the
+// ties), and stops once topk pools are kept.
 template <typename Map>
-__device__ void select_streaming(SelectSmem& s, const float* __restrict__ sc, int n, int topk, const Map& map, int r,
-                                 int tail, int32_t* __restrict__ row, int W) {
-    const int t = threadIdx.x;
-    // ---- level 1: bits 31..20 over all keys
-    for (int b = t; b < HIST_BINS; b += SEL_THREADS) s.hist[b] = 0;
+__device__ __forceinline__ void select_chunked(SelectSmem& s, uint32_t* cand, int cand_cap,
+                                               const float* __restrict__ sc, int n, int topk, const Map& map,
+                                               int32_t* __restrict__ row) {
+    const int t = threadIdx.x, wid = t >> 5, lane = t & 31;
+    const uint32_t below = (1u << lane) - 1u;
+    const uint32_t* tab = s.hist;
+    chunk_level(s, sc, n, 0u, 0u, 21, 2048, (uint32_t)topk);
+    uint32_t prefix = s.digit << 21;
+    uint32_t rem = s.remaining, cnt = s.hist[s.digit & 2047u];
     if (t == 0) s.n_cand = 0;
     __syncthreads();
-    for (int p = t; p < n; p += SEL_THREADS) atomicAdd(&s.hist[score_key(sc[p]) >> 20], 1u);
-    __syncthreads();
-    pick_digit(s, HIST_BINS, (uint32_t)topk);
-    uint32_t prefix = s.digit << 20;
-    uint32_t remaining = s.remaining;
-    // candidates of the chosen bin
-    for (int p = t; p < n; p += SEL_THREADS) {
-        const uint32_t key = score_key(sc[p]);
-        if ((key >> 20) == (prefix >> 20)) {
-            const uint32_t slot = atomicAdd(&s.n_cand, 1u);
-            if (slot < CAND_CAP) s.cand_key[slot] = key;
+    bool whole = cnt == rem;
+    const uint32_t n_list = cnt;                     // keys in the chosen level-1 bin
+    const bool listed = cand != nullptr && n_list <= (uint32_t)cand_cap;
+    if (!whole && listed) {                          // copy the bin's keys, one atomic per warp and column
+        for (int c0 = 0; c0 < n; c0 += FAST_MAX) {
+            uint32_t key[FAST_KPT], valid;
+            load_chunk(sc, n, c0, key, valid);
+#pragma unroll
+            for (int j = 0; j < FAST_KPT; ++j) {
+                const bool m = ((valid >> j) & 1u) && (key[j] >> 21) == (prefix >> 21);
+                const uint32_t b = __ballot_sync(0xffffffffu, m);
+                if (b != 0u) {
+                    const int leader = __ffs(b) - 1;
+                    uint32_t base = 0;
+                    if (lane == leader) base = atomicAdd(&s.n_cand, (uint32_t)__popc(b));
+                    base = __shfl_sync(0xffffffffu, base, leader);
+                    if (m) cand[base + __popc(b & below)] = key[j];
+                }
+            }
         }
+        __syncthreads();
     }
-    __syncthreads();
-    const uint32_t nc = s.n_cand;
-    const bool from_list = nc <= CAND_CAP;
-
-    // ---- level 2: bits 19..8 among keys matching bits 31..20
-    for (int b = t; b < HIST_BINS; b += SEL_THREADS) s.hist[b] = 0;
-    __syncthreads();
-    if (from_list) {
-        for (uint32_t c = t; c < nc; c += SEL_THREADS) atomicAdd(&s.hist[(s.cand_key[c] >> 8) & 0xfffu], 1u);
-    } else {
-        for (int p = t; p < n; p += SEL_THREADS) {
-            const uint32_t key = score_key(sc[p]);
-            if ((key >> 20) == (prefix >> 20)) atomicAdd(&s.hist[(key >> 8) & 0xfffu], 1u);
-        }
+    if (!whole) {
+        if (listed) list_level(s, cand, n_list, 0xFFE00000u, prefix, 10, 2048, rem);
+        else chunk_level(s, sc, n, 0xFFE00000u, prefix, 10, 2048, rem);
+        prefix |= s.digit << 10;
+        rem = s.remaining;
+        cnt = s.hist[s.digit & 2047u];
+        __syncthreads();
+        whole = cnt == rem;
     }
-    __syncthreads();
-    pick_digit(s, HIST_BINS, remaining);
-    prefix |= s.digit << 8;
-    remaining = s.remaining;
-
-    // ---- level 3: bits 7..0 among keys matching bits 31..8
-    for (int b = t; b < 256; b += SEL_THREADS) s.hist[b] = 0;
-    __syncthreads();
-    if (from_list) {
-        for (uint32_t c = t; c < nc; c += SEL_THREADS) {
-            const uint32_t key = s.cand_key[c];
-            if ((key >> 8) == (prefix >> 8)) atomicAdd(&s.hist[key & 0xffu], 1u);
-        }
-    } else {
-        for (int p = t; p < n; p += SEL_THREADS) {
-            const uint32_t key = score_key(sc[p]);
-            if ((key >> 8) == (prefix >> 8)) atomicAdd(&s.hist[key & 0xffu], 1u);
-        }
+    uint32_t K = prefix, need_eq = 0, n_eq = 0;
+    if (!whole) {
+        if (listed) list_level(s, cand, n_list, 0xFFFFFC00u, prefix, 0, 1024, rem);
+        else chunk_level(s, sc, n, 0xFFFFFC00u, prefix, 0, 1024, rem);
+        K = prefix | s.digit;
+        need_eq = s.remaining;
+        n_eq = s.hist[s.digit & 1023u];
+        __syncthreads();
     }
-    __syncthreads();
-    pick_digit(s, 256, remaining);
-    const uint32_t K = prefix | s.digit;
-    const int need_eq = (int)s.remaining;
-
-    // ---- ordered compaction: positions of the kept pools, ascending
-    int sel_base = 0, eq_base = 0;
-    for (int c0 = 0; c0 < n; c0 += SEL_THREADS) {
-        const int p = c0 + t;
-        const uint32_t key = p < n ? score_key(sc[p]) : 0u;
-        const int gt = (p < n) && key > K;
-        const int eq = (p < n) && key == K;
-        int eq_tot, sel_tot;
-        const int eq_rank = eq_base + block_excl_scan(eq, s.warp_tot, eq_tot);
-        const int take = gt || (eq && eq_rank < need_eq);
-        const int slot = sel_base + block_excl_scan(take, s.warp_tot, sel_tot);
-        if (take && slot < topk) {
-            const int pos = map.pool(p);
-            *reinterpret_cast<int4*>(row + KPOOL * slot) = make_int4(pos, pos + 1, pos + 2, pos + 3);
+    const bool ties = n_eq != need_eq;
+    int sel_base = 0;
+    uint32_t eq_base = 0;
+    for (int c0 = 0; c0 < n && sel_base < topk; c0 += FAST_MAX) {
+        uint32_t key[FAST_KPT], valid;
+        load_chunk(sc, n, c0, key, valid);
+        uint32_t gt = 0, eq = 0;
+#pragma unroll
+        for (int j = 0; j < FAST_KPT; ++j) {
+            const bool v = (valid >> j) & 1u;
+            gt |= (v && (whole ? key[j] >= K : key[j] > K) ? 1u : 0u) << j;
+            eq |= (v && !whole && key[j] == K ? 1u : 0u) << j;
         }
-        sel_base += sel_tot;
-        eq_base += eq_tot;
-    }
-    for (int j = KPOOL * topk + t; j < W; j += SEL_THREADS) {
-        const int q = j - KPOOL * topk;
-        row[j] = q < tail ? map.tok(r - tail + 1 + q) : -1;
+        uint32_t take = gt | eq;
+        if (ties) {                                  // the lowest pool indices among the ties win
+            const int eq_tot = column_scan<FAST_KPT>(s, eq);
+#pragma unroll
+            for (int j = 0; j < FAST_KPT; ++j) {
+                const uint32_t b = __ballot_sync(0xffffffffu, (eq >> j) & 1u);
+                if (((eq >> j) & 1u) && eq_base + tab[8 * j + wid] + __popc(b & below) >= need_eq)
+                    take &= ~(1u << j);
+            }
+            __syncthreads();
+            eq_base += (uint32_t)eq_tot;
+        }
+        const int take_tot = column_scan<FAST_KPT>(s, take);
+#pragma unroll
+        for (int j = 0; j < FAST_KPT; ++j) {
+            const uint32_t b = __ballot_sync(0xffffffffu, (take >> j) & 1u);
+            const int rank = sel_base + (int)(tab[8 * j + wid] + __popc(b & below));
+            if (((take >> j) & 1u) && rank < topk) {
+                const int pos = map.pool(c0 + SEL_THREADS * j + t);
+                *reinterpret_cast<int4*>(row + KPOOL * rank) = make_int4(pos, pos + 1, pos + 2, pos + 3);
+            }
+        }
+        __syncthreads();                             // tab is reused by the next chunk
+        sel_base += take_tot;
     }
 }
 
@@ -363,10 +430,21 @@ __device__ __forceinline__ bool fast_row(const RowInfo& ri, int topk) {
     return ri.d >= 0 && ri.n > topk && ri.n <= FAST_MAX;
 }
 
+constexpr int MID_MAX = 2 * ROWBUF - 8;               // pools of a row that fits both row buffers
+
+__device__ __forceinline__ bool mid_row(const RowInfo& ri, int topk) {
+    return ri.d >= 0 && ri.n > topk && ri.n > FAST_MAX && ri.n <= MID_MAX;
+}
+
+constexpr int SEL_CTAS_PER_SM = 3;                   // 3 x (65.6 KB row buffers + 8.2 KB) of shared memory
+
 // Persistent: block b walks rows b, b + gridDim.x, ...; the scores of the
 // next row are copied into shared memory (cp.async) while the current row is
 // ranked, so the load latency of a row is hidden behind the previous one.
-__global__ void __launch_bounds__(SEL_THREADS, 2) select_kernel(const float* __restrict__ scores,
+// A row longer than one row buffer but not two is copied into both when its
+// turn comes (the next row's copy then starts after it); longer rows are read
+// from global memory.
+__global__ void __launch_bounds__(SEL_THREADS, SEL_CTAS_PER_SM) select_kernel(const float* __restrict__ scores,
                                                              const int64_t* __restrict__ pair_base,
                                                              const int32_t* __restrict__ cu_seqlens,
                                                              const int32_t* __restrict__ cu_pools,
@@ -384,10 +462,10 @@ __global__ void __launch_bounds__(SEL_THREADS, 2) select_kernel(const float* __r
         const int i2 = i + (int)gridDim.x;
         RowInfo nxt;
         nxt.d = -1;
-        if (i2 < T) {
-            nxt = row_info(i2, pair_base, cu_seqlens, cu_pools, tok_doc, n_docs);
-            if (fast_row(nxt, topk)) prefetch_row(rowbuf + ((k + 1) & 1) * ROWBUF, scores, nxt.start, nxt.n);
-        }
+        if (i2 < T) nxt = row_info(i2, pair_base, cu_seqlens, cu_pools, tok_doc, n_docs);
+        const bool cur_mid = mid_row(cur, topk);
+        const bool pf_nxt = fast_row(nxt, topk);
+        if (pf_nxt && !cur_mid) prefetch_row(rowbuf + ((k + 1) & 1) * ROWBUF, scores, nxt.start, nxt.n);
         asm volatile("cp.async.commit_group;\n" ::: "memory");
 
         int32_t* row = indices + (int64_t)i * W;
@@ -396,21 +474,33 @@ __global__ void __launch_bounds__(SEL_THREADS, 2) select_kernel(const float* __r
             for (int j = t; j < W; j += SEL_THREADS) row[j] = -1;
         } else if (cur.n <= topk) {                   // every candidate is kept: the causal prefix
             for (int j = t; j < W; j += SEL_THREADS) row[j] = (j <= cur.r) ? map.tok(j) : -1;
-        } else if (cur.n <= FAST_MAX) {
-            asm volatile("cp.async.wait_group 1;\n" ::: "memory");
-            __syncthreads();
-            const float* sc = rowbuf + (k & 1) * ROWBUF + (int)(cur.start & 3);
-            if (cur.n <= 8 * SEL_THREADS) select_registers<8>(s, sc, cur.n, topk, map, row);
-            else if (cur.n <= 16 * SEL_THREADS) select_registers<16>(s, sc, cur.n, topk, map, row);
-            else select_registers<32>(s, sc, cur.n, topk, map, row);
+        } else {
+            if (cur.n <= FAST_MAX) {
+                asm volatile("cp.async.wait_group 1;\n" ::: "memory");
+                __syncthreads();
+                const float* sc = rowbuf + (k & 1) * ROWBUF + (int)(cur.start & 3);
+                if (cur.n <= 8 * SEL_THREADS) select_registers<8>(s, sc, cur.n, topk, map, row);
+                else if (cur.n <= 16 * SEL_THREADS) select_registers<16>(s, sc, cur.n, topk, map, row);
+                else select_registers<32>(s, sc, cur.n, topk, map, row);
+            } else if (cur_mid) {                     // no copy is in flight: this row was not prefetched
+                prefetch_row(rowbuf, scores, cur.start, cur.n);
+                asm volatile("cp.async.commit_group;\n" ::: "memory");
+                asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+                __syncthreads();
+                select_chunked(s, nullptr, 0, rowbuf + (int)(cur.start & 3), cur.n, topk, map, row);
+            } else {
+                // a row too long for the row buffers leaves its own buffer free for the candidate list
+                uint32_t* cand = reinterpret_cast<uint32_t*>(rowbuf + (k & 1) * ROWBUF);
+                select_chunked(s, cand, FAST_MAX, scores + cur.start, cur.n, topk, map, row);
+            }
             for (int j = KPOOL * topk + t; j < W; j += SEL_THREADS) {
                 const int q = j - KPOOL * topk;
                 row[j] = q < cur.tail ? map.tok(cur.r - cur.tail + 1 + q) : -1;
             }
-        } else {
-            select_streaming(s, scores + cur.start, cur.n, topk, map, cur.r, cur.tail, row, W);
         }
         __syncthreads();                              // the row buffer and s are reused
+        if (pf_nxt && cur_mid) prefetch_row(rowbuf + ((k + 1) & 1) * ROWBUF, scores, nxt.start, nxt.n);
+        asm volatile("cp.async.commit_group;\n" ::: "memory");
         cur = nxt;
     }
     asm volatile("cp.async.wait_group 0;\n" ::: "memory");
@@ -420,12 +510,13 @@ __global__ void __launch_bounds__(SEL_THREADS, 2) select_kernel(const float* __r
 // (position r = seq_lens[b] - 1).  Its n = seq_lens[b] / 4 complete pools have
 // scores at scores[b * stride + p]; positions map to latent-cache slots through
 // the sequence's row of the block table.
-__global__ void __launch_bounds__(SEL_THREADS) decode_select_kernel(const float* __restrict__ scores, int64_t stride,
+__global__ void __launch_bounds__(SEL_THREADS, 2) decode_select_kernel(const float* __restrict__ scores, int64_t stride,
                                                                     const int32_t* __restrict__ seq_lens,
                                                                     const int32_t* __restrict__ block_table,
                                                                     int max_pages, int topk,
                                                                     int32_t* __restrict__ indices, int W) {
     __shared__ SelectSmem s;
+    __shared__ uint32_t cand[DECODE_CAND_CAP];
     const int t = threadIdx.x, b = blockIdx.x;
     const int L = seq_lens[b];
     int32_t* row = indices + (int64_t)b * W;
@@ -436,16 +527,15 @@ __global__ void __launch_bounds__(SEL_THREADS) decode_select_kernel(const float*
         for (int j = t; j < W; j += SEL_THREADS) row[j] = -1;
     } else if (n <= topk) {
         for (int j = t; j < W; j += SEL_THREADS) row[j] = (j <= r) ? map.tok(j) : -1;
-    } else if (n <= FAST_MAX) {
+    } else {
         if (n <= 8 * SEL_THREADS) select_registers<8>(s, sc, n, topk, map, row);
         else if (n <= 16 * SEL_THREADS) select_registers<16>(s, sc, n, topk, map, row);
-        else select_registers<32>(s, sc, n, topk, map, row);
+        else if (n <= FAST_MAX) select_registers<32>(s, sc, n, topk, map, row);
+        else select_chunked(s, cand, DECODE_CAND_CAP, sc, n, topk, map, row);
         for (int j = KPOOL * topk + t; j < W; j += SEL_THREADS) {
             const int q = j - KPOOL * topk;
             row[j] = q < tail ? map.tok(r - tail + 1 + q) : -1;
         }
-    } else {
-        select_streaming(s, sc, n, topk, map, r, tail, row, W);
     }
 }
 
@@ -467,11 +557,14 @@ int launch_select(const float* scores, const int64_t* pair_base, const kpool_lay
     if (n_sm[dev] == 0) {
         if (cudaFuncSetAttribute(select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kDyn) != cudaSuccess)
             return KPOOL_ERR_CUDA;
+        // the whole carveout as shared memory, so SEL_CTAS_PER_SM blocks fit on an SM
+        if (cudaFuncSetAttribute(select_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100) != cudaSuccess)
+            return KPOOL_ERR_CUDA;
         int sms = 0;
         if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return KPOOL_ERR_CUDA;
         n_sm[dev] = sms;
     }
-    const int grid = L.T < 2 * n_sm[dev] ? L.T : 2 * n_sm[dev];
+    const int grid = L.T < SEL_CTAS_PER_SM * n_sm[dev] ? L.T : SEL_CTAS_PER_SM * n_sm[dev];
     select_kernel<<<grid, SEL_THREADS, kDyn, stream>>>(scores, pair_base, L.cu_seqlens, L.cu_pools, L.tok_doc,
                                                       L.n_docs, L.T, topk, indices, W);
     return cudaGetLastError() == cudaSuccess ? KPOOL_OK : KPOOL_ERR_CUDA;

@@ -284,7 +284,7 @@ class DecodeWorkload:
 def decode_workload(idx: int) -> DecodeWorkload:
     if idx == 0:      # tiny: every branch of a row (all pools kept, radix select, tails 0..3, several pages)
         return DecodeWorkload("decode_tiny", 50, (5, 9, 130, 517, 1029, 1100, 2052, 2175), topk=64)
-    if idx == 1:      # rows of > 8192 pools take the streaming select
+    if idx == 1:      # rows of > 8192 pools take the chunked select
         return DecodeWorkload("decode_long_rows", 51, (33000, 40003, 4099))
     if idx == 2:      # benchmark: 128 sequences, lengths log-uniform in [4096, 32768]
         rng = np.random.default_rng([52, _DEC_LENS])

@@ -201,6 +201,75 @@ def test_stage_select_ties(kind):
     np.testing.assert_array_equal(got, want)
 
 
+def _long_row_select(lens, kind, min_n, seed):
+    """Stage select over one compact score triangle of documents `lens` (standard normal scores), the
+    rows of more than min_n pools overwritten with the pattern `kind`; compares those rows and 200
+    others with the oracle."""
+    wl = workloads.custom("long_rows", seed, lens, topk=512)
+    lay_o = O.pool_layout(wl.cu_seqlens)
+    cu = wl.cu_seqlens
+    pair_base = np.zeros(len(cu), np.int64)
+    for d in range(len(cu) - 1):
+        a, b = divmod(int(cu[d + 1] - cu[d]), 4)
+        pair_base[d + 1] = pair_base[d] + 2 * a * (a - 1) + a * (b + 1)
+    rng = np.random.default_rng(seed)
+    buf = rng.standard_normal(int(pair_base[-1]), dtype=np.float32)
+
+    def start(i):
+        d, r, n_i, _ = O.query_geometry(lay_o, i)
+        a, b = divmod(r, 4)
+        return int(pair_base[d]) + 2 * a * (a - 1) + a * (b + 1), n_i
+
+    long_rows = [i for i in range(wl.T) if O.query_geometry(lay_o, i)[2] > min_n]
+    assert len(long_rows) > 200
+    for i in long_rows:
+        s0, n = start(i)
+        if kind == "ties_across_chunks":             # 100 pools above the tie, 700 tied, 300 of them in chunk 0
+            x = -np.abs(rng.standard_normal(n)).astype(np.float32)
+            pick = rng.permutation(8192)[:300]
+            x[pick] = 1.0
+            late = 8192 + rng.permutation(n - 8192)[:500]
+            x[late[:400]] = 1.0
+            x[late[400:]] = 2.0
+        elif kind == "increasing":                   # every kept pool in the last chunk
+            x = np.arange(n, dtype=np.float32) * np.float32(0.001)
+        elif kind == "all_equal":
+            x = np.full(n, -3.5, np.float32)
+        else:
+            continue
+        buf[s0:s0 + n] = x
+    check = long_rows + sorted(rng.choice(np.setdiff1d(np.arange(wl.T), long_rows), 200, replace=False).tolist())
+    cu_d = torch.from_numpy(cu).cuda()
+    p = KP.params_of(wl)
+    k = torch.zeros((wl.T, wl.d_idx), dtype=torch.bfloat16, device="cuda")
+    gate = torch.zeros((wl.T, wl.d_idx), dtype=torch.float32, device="cuda")
+    ape = torch.zeros((4, wl.d_idx), dtype=torch.float32, device="cuda")
+    _, lay = K.kpool_build(k, gate, ape, cu_d, p)
+    W = K.row_width(wl.topk)
+    got = K.stage_select(torch.from_numpy(buf).cuda(), torch.from_numpy(pair_base).cuda(), lay, wl.topk,
+                         W=W).cpu().numpy()
+    for i in check:
+        s0, n = start(i)
+        want = O.index_row(lay_o, i, O.select_pools(buf[s0:s0 + n], wl.topk), W)
+        np.testing.assert_array_equal(got[i], want, err_msg=f"row {i} (n = {n})")
+
+
+@pytest.mark.parametrize("kind", ["normal", "ties_across_chunks", "increasing", "all_equal"])
+def test_stage_select_rows_longer_than_8192_pools(kind):
+    """Rows of 8193 to 16392 candidate pools (documents of 32769 to 65571 tokens) are copied whole into
+    shared memory and ranked in chunks of 8192 pools.  The patterns put the kept pools in the first
+    chunk only, in the second only, or split the tie at the threshold across both."""
+    _long_row_select((4 * (8192 + 700) + 2, 1001), kind, 8192, 81)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("kind", ["normal", "ties_across_chunks"])
+def test_stage_select_rows_longer_than_16392_pools(kind):
+    """Rows of more than 16392 candidate pools (documents of more than 65571 tokens) are read from
+    global memory on every pass, with the keys of the chosen level-1 bin in a shared candidate list."""
+    _long_row_select((4 * (16392 + 60) + 3,), kind, 16392, 82)
+
+
 # ----------------------------------------------------------------- edge cases
 
 @pytest.mark.parametrize("lens", [(1,), (3,), (4,), (5, 0, 7), (2, 1, 3, 2), (130, 0, 0, 257), (4096 + 3,)])
