@@ -117,18 +117,16 @@ constexpr int FAST_KPT = 32;                          // keys per thread on the 
 constexpr int FAST_MAX = SEL_THREADS * FAST_KPT;     // 8192 candidate pools
 
 // One radix level over register-held keys: histogram of bits [shift, shift+log2(nbins)) of the
-// valid keys whose bits above match `prefix` under `hi_mask`, then the digit that holds the
+// keys whose bits above match `prefix` under `hi_mask`, then the digit that holds the
 // remaining-th largest key (s.digit, s.remaining).
 template <int NC>
-__device__ __forceinline__ void fast_level(SelectSmem& s, const uint32_t (&key)[NC], uint32_t valid,
-                                           uint32_t hi_mask, uint32_t prefix, int shift, int nbins,
-                                           uint32_t remaining) {
+__device__ __forceinline__ void fast_level(SelectSmem& s, const uint32_t (&key)[NC], uint32_t hi_mask,
+                                           uint32_t prefix, int shift, int nbins, uint32_t remaining) {
     for (int b = threadIdx.x; b < nbins; b += SEL_THREADS) s.hist[b] = 0;
     __syncthreads();
 #pragma unroll
     for (int j = 0; j < NC; ++j)
-        if (((valid >> j) & 1u) && (key[j] & hi_mask) == prefix)
-            atomicAdd(&s.hist[(key[j] >> shift) & (uint32_t)(nbins - 1)], 1u);
+        if ((key[j] & hi_mask) == prefix) atomicAdd(&s.hist[(key[j] >> shift) & (uint32_t)(nbins - 1)], 1u);
     __syncthreads();
     pick_digit(s, nbins, remaining);
 }
@@ -162,7 +160,6 @@ __device__ void select_registers(SelectSmem& s, const float* __restrict__ sc, in
     const uint32_t below = (1u << (t & 31)) - 1u;
     const uint32_t* tab = s.hist;
     uint32_t key[NC];
-    uint32_t valid = 0;
     // every load first, then the conversions: with sc in global memory (paged decode) the loads
     // are then all in flight together instead of one round trip per key
     float raw[NC];
@@ -171,22 +168,26 @@ __device__ void select_registers(SelectSmem& s, const float* __restrict__ sc, in
         const int p = SEL_THREADS * j + t;
         raw[j] = p < n ? sc[p] : 0.f;
     }
+    // Slots past the row (p >= n) get key 0, the key of NaN and the lowest there is, and take part
+    // in every count.  They change nothing: with n > topk valid keys the topk-th largest key is
+    // that of a valid pool; if it is 0, the slots past the row tie with it at the highest pool
+    // indices, so the need_eq lowest-indexed ties are all valid; and the bin of key 0 can never be
+    // kept whole (that would need n + the slots past the row <= topk).
 #pragma unroll
     for (int j = 0; j < NC; ++j) {
         const int p = SEL_THREADS * j + t;
         key[j] = p < n ? score_key(raw[j]) : 0u;
-        valid |= (p < n ? 1u : 0u) << j;
     }
     // Radix levels over bits 31..21, 20..10, 9..0.  When the bin that holds the
     // topk-th key is kept whole (its count equals the keys still needed), every
     // key from the bin's lowest value up is kept and the later levels are skipped.
-    fast_level(s, key, valid, 0u, 0u, 21, 2048, (uint32_t)topk);
+    fast_level(s, key, 0u, 0u, 21, 2048, (uint32_t)topk);
     uint32_t prefix = s.digit << 21;
     uint32_t rem = s.remaining, cnt = s.hist[s.digit & 2047u];
     __syncthreads();                                 // every thread has read the bin before it is reused
     bool whole = cnt == rem;
     if (!whole) {
-        fast_level(s, key, valid, 0xFFE00000u, prefix, 10, 2048, rem);
+        fast_level(s, key, 0xFFE00000u, prefix, 10, 2048, rem);
         prefix |= s.digit << 10;
         rem = s.remaining;
         cnt = s.hist[s.digit & 2047u];
@@ -195,7 +196,7 @@ __device__ void select_registers(SelectSmem& s, const float* __restrict__ sc, in
     }
     uint32_t K = prefix, need_eq = 0, n_eq = 0;      // whole bin: keep every key >= K
     if (!whole) {
-        fast_level(s, key, valid, 0xFFFFFC00u, prefix, 0, 1024, rem);
+        fast_level(s, key, 0xFFFFFC00u, prefix, 0, 1024, rem);
         K = prefix | s.digit;
         need_eq = s.remaining;
         n_eq = s.hist[s.digit & 1023u];              // keys equal to K
@@ -205,9 +206,8 @@ __device__ void select_registers(SelectSmem& s, const float* __restrict__ sc, in
     uint32_t gt = 0, eq = 0;
 #pragma unroll
     for (int j = 0; j < NC; ++j) {
-        const bool v = (valid >> j) & 1u;
-        gt |= (v && (whole ? key[j] >= K : key[j] > K) ? 1u : 0u) << j;
-        eq |= (v && !whole && key[j] == K ? 1u : 0u) << j;
+        gt |= ((whole ? key[j] >= K : key[j] > K) ? 1u : 0u) << j;
+        eq |= (!whole && key[j] == K ? 1u : 0u) << j;
     }
     uint32_t take = gt | eq;
     // the column ballots are taken again where the ranks are read: keeping them costs NC registers
@@ -234,21 +234,19 @@ __device__ void select_registers(SelectSmem& s, const float* __restrict__ sc, in
 
 }  // namespace
 
-// Keys of chunk c0 (pools c0 + 256j + t in key j) of a row in global memory.
-__device__ __forceinline__ void load_chunk(const float* __restrict__ sc, int n, int c0, uint32_t (&key)[FAST_KPT],
-                                           uint32_t& valid) {
+// Keys of chunk c0 (pools c0 + 256j + t in key j) of a row; slots past the row get key 0, as on
+// the register path (and for the same reason change nothing).
+__device__ __forceinline__ void load_chunk(const float* __restrict__ sc, int n, int c0, uint32_t (&key)[FAST_KPT]) {
     float raw[FAST_KPT];
 #pragma unroll
     for (int j = 0; j < FAST_KPT; ++j) {
         const int p = c0 + SEL_THREADS * j + (int)threadIdx.x;
         raw[j] = p < n ? sc[p] : 0.f;
     }
-    valid = 0;
 #pragma unroll
     for (int j = 0; j < FAST_KPT; ++j) {
         const int p = c0 + SEL_THREADS * j + (int)threadIdx.x;
         key[j] = p < n ? score_key(raw[j]) : 0u;
-        valid |= (p < n ? 1u : 0u) << j;
     }
 }
 
@@ -258,12 +256,11 @@ __device__ __forceinline__ void chunk_level(SelectSmem& s, const float* __restri
     for (int b = threadIdx.x; b < nbins; b += SEL_THREADS) s.hist[b] = 0;
     __syncthreads();
     for (int c0 = 0; c0 < n; c0 += FAST_MAX) {
-        uint32_t key[FAST_KPT], valid;
-        load_chunk(sc, n, c0, key, valid);
+        uint32_t key[FAST_KPT];
+        load_chunk(sc, n, c0, key);
 #pragma unroll
         for (int j = 0; j < FAST_KPT; ++j)
-            if (((valid >> j) & 1u) && (key[j] & hi_mask) == prefix)
-                atomicAdd(&s.hist[(key[j] >> shift) & (uint32_t)(nbins - 1)], 1u);
+            if ((key[j] & hi_mask) == prefix) atomicAdd(&s.hist[(key[j] >> shift) & (uint32_t)(nbins - 1)], 1u);
     }
     __syncthreads();
     pick_digit(s, nbins, remaining);
@@ -305,11 +302,11 @@ __device__ __forceinline__ void select_chunked(SelectSmem& s, uint32_t* cand, in
     const bool listed = cand != nullptr && n_list <= (uint32_t)cand_cap;
     if (!whole && listed) {                          // copy the bin's keys, one atomic per warp and column
         for (int c0 = 0; c0 < n; c0 += FAST_MAX) {
-            uint32_t key[FAST_KPT], valid;
-            load_chunk(sc, n, c0, key, valid);
+            uint32_t key[FAST_KPT];
+            load_chunk(sc, n, c0, key);
 #pragma unroll
             for (int j = 0; j < FAST_KPT; ++j) {
-                const bool m = ((valid >> j) & 1u) && (key[j] >> 21) == (prefix >> 21);
+                const bool m = (key[j] >> 21) == (prefix >> 21);
                 const uint32_t b = __ballot_sync(0xffffffffu, m);
                 if (b != 0u) {
                     const int leader = __ffs(b) - 1;
@@ -344,14 +341,13 @@ __device__ __forceinline__ void select_chunked(SelectSmem& s, uint32_t* cand, in
     int sel_base = 0;
     uint32_t eq_base = 0;
     for (int c0 = 0; c0 < n && sel_base < topk; c0 += FAST_MAX) {
-        uint32_t key[FAST_KPT], valid;
-        load_chunk(sc, n, c0, key, valid);
+        uint32_t key[FAST_KPT];
+        load_chunk(sc, n, c0, key);
         uint32_t gt = 0, eq = 0;
 #pragma unroll
         for (int j = 0; j < FAST_KPT; ++j) {
-            const bool v = (valid >> j) & 1u;
-            gt |= (v && (whole ? key[j] >= K : key[j] > K) ? 1u : 0u) << j;
-            eq |= (v && !whole && key[j] == K ? 1u : 0u) << j;
+            gt |= ((whole ? key[j] >= K : key[j] > K) ? 1u : 0u) << j;
+            eq |= (!whole && key[j] == K ? 1u : 0u) << j;
         }
         uint32_t take = gt | eq;
         if (ties) {                                  // the lowest pool indices among the ties win

@@ -179,11 +179,12 @@ def test_stage_select_bit_exact_on_oracle_scores():
     np.testing.assert_array_equal(got, want)
 
 
-@pytest.mark.parametrize("kind", ["few_values", "zeros_signed", "all_equal", "negative"])
+@pytest.mark.parametrize("kind", ["few_values", "zeros_signed", "all_equal", "negative", "nan_and_inf"])
 def test_stage_select_ties(kind):
     wl = workloads.custom("ties", 7, (1500, 1037, 3), topk=64)
     lay_o = O.pool_layout(wl.cu_seqlens)
-    rng = np.random.default_rng({"few_values": 1, "zeros_signed": 2, "all_equal": 3, "negative": 4}[kind])
+    rng = np.random.default_rng({"few_values": 1, "zeros_signed": 2, "all_equal": 3, "negative": 4,
+                                 "nan_and_inf": 5}[kind])
     S = []
     for i in range(wl.T):
         n = O.query_geometry(lay_o, i)[2]
@@ -194,6 +195,10 @@ def test_stage_select_ties(kind):
             s[rng.random(n) < 0.05] = 1.0
         elif kind == "all_equal":
             s = np.full(n, 3.5, np.float32)
+        elif kind == "nan_and_inf":                  # NaN ranks lowest: long rows keep some NaN pools
+            s = rng.standard_normal(n).astype(np.float32)
+            s[rng.random(n) < 0.85] = np.nan
+            s[rng.random(n) < 0.02] = np.inf
         else:
             s = -np.abs(rng.standard_normal(n)).astype(np.float32)
         S.append(s)
