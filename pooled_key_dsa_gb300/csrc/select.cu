@@ -5,7 +5,7 @@
 // incomplete pool; index rows are padded to a multiple of 128.  NeMo AutoModel
 // PR "add GLM-5.3-Flash training support": 2048 + 3 = 2051 raw slots.
 //
-// One 256-thread block per query row.  Scores become order-preserving uint32
+// A 256-thread block ranks one query row at a time.  Scores become order-preserving uint32
 // keys.  Rows of up to 8192 candidate pools (every row of a document of up to
 // 32768 tokens) take the register path: each thread holds 32 keys (pools
 // t, t+256, ...; loads coalesced), a three-level radix select (bits 31..21,
