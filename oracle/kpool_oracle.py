@@ -244,11 +244,13 @@ def scores_exact(q_idx, w, kpool, layout, rows) -> list[np.ndarray]:
 def select_pools(S_row: np.ndarray, topk: int) -> np.ndarray:
     """Indices (relative to the document's first pool) of the top
     min(topk, n) pools by score descending, ties to the lower pool index;
-    -0 is +0 and NaN ranks lowest.  Returned in ascending pool order."""
+    -0 is +0 and NaN ranks lowest, below -inf.  Returned in ascending pool
+    order."""
     S = np.asarray(S_row, dtype=np.float64) + 0.0
-    S = np.where(np.isnan(S), -np.inf, S)
+    nan = np.isnan(S)
+    S = np.where(nan, -np.inf, S)
     n = len(S)
-    order = np.lexsort((np.arange(n), -S))       # primary: -S ascending, then pool
+    order = np.lexsort((np.arange(n), -S, nan))  # primary: numbers first, then -S ascending, then pool
     return np.sort(order[:min(topk, n)])
 
 

@@ -199,6 +199,7 @@ def test_stage_select_ties(kind):
             s = rng.standard_normal(n).astype(np.float32)
             s[rng.random(n) < 0.85] = np.nan
             s[rng.random(n) < 0.02] = np.inf
+            s[rng.random(n) < 0.05] = -np.inf          # below every number but above NaN
         else:
             s = -np.abs(rng.standard_normal(n)).astype(np.float32)
         S.append(s)

@@ -234,6 +234,14 @@ def test_zero_weights_pick_lowest_pools():
     assert O.select_pools(S, 8).tolist() == list(range(8))
 
 
+def test_select_nan_ranks_below_every_number():
+    """NaN is below -inf (reading R6: NaN ranks lowest); among NaNs the lower pool index wins."""
+    S = np.array([np.nan, -np.inf, np.nan, -3e38, np.inf, np.nan, 0.0], np.float32)
+    assert O.select_pools(S, 4).tolist() == [1, 3, 4, 6]
+    assert O.select_pools(S, 5).tolist() == [0, 1, 3, 4, 6]
+    assert O.select_pools(S, 6).tolist() == [0, 1, 2, 3, 4, 6]
+
+
 def test_select_positive_scaling_invariant():
     rng = np.random.default_rng(8)
     S = rng.standard_normal(300).astype(np.float32)
