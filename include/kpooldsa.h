@@ -145,7 +145,8 @@ int kpool_build(const void* k, const float* gate, const float* ape, const int32_
  *              then -1.  W >= 4*topk + 3 and a multiple of 4 (2176 for topk
  *              512 keeps rows a multiple of 128); 16-byte aligned.
  * Score of query i for pool p: s_k[p] * sum_h w[i,h] s_q[i,h] ReLU(q8[i,h].k8[p]);
- * ties go to the lower pool index.
+ * ties go to the lower pool index, -0 ranks as +0, and a NaN score ranks below
+ * every number (-inf included).
  * Source: prime-rl PR "GLM-5.3-Flash text model", Summary. */
 int dsa_index(const void* q_idx, const float* w, const float* kpool, const kpool_layout* layout,
               int32_t topk, const kpool_params* p, void* workspace, size_t workspace_bytes,
@@ -260,7 +261,8 @@ int dsa_index_noalloc(const void* q_idx, const float* w, const float* kpool, con
                       int32_t topk, const kpool_params* p, int32_t* indices, int32_t W, kpool_stream_t stream);
 
 /* Stage entry point: top-k select + row expansion alone, fed with scores in
- * the workspace's compact layout (same rules as dsa_index's last step).
+ * the workspace's compact layout (same rules as dsa_index's last step,
+ * including the order of ties, signed zeros and NaN).
  *   scores   fp32, compact triangle as described for kpool_ws_offsets
  *            (16-byte aligned, as the workspace's scores are)
  *   pair_base int64 [n_docs+1] as described there (8-byte aligned) */
