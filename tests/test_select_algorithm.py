@@ -38,17 +38,7 @@ def _kernel_select(scores: np.ndarray, topk: int, pad_to: int = 256) -> np.ndarr
     n_pad = -(-n // pad_to) * pad_to
     key = np.zeros(n_pad, np.uint64)
     key[:n] = _keys(scores)                         # the slots past the row keep key 0
-    levels = ((0x00000000, 21, 2048), (0xFFE00000, 10, 2048), (0xFFFFFC00, 0, 1024))
-    prefix, rem, whole = 0, topk, False
-    for hi_mask, shift, nbins in levels:
-        inbin = (key & hi_mask) == prefix
-        hist = np.bincount(((key[inbin] >> shift) & (nbins - 1)).astype(np.int64), minlength=nbins)
-        d, rem = _pick(hist, rem)
-        prefix |= d << shift
-        if int(hist[d]) == rem and shift > 0:       # the bin is kept whole
-            whole = True
-            break
-    K = prefix
+    K, whole, rem = _threshold(key, topk)
     if whole:
         take = key >= K
     else:
@@ -59,6 +49,46 @@ def _kernel_select(scores: np.ndarray, topk: int, pad_to: int = 256) -> np.ndarr
     kept = kept[kept < n]
     assert len(kept) == topk, (len(kept), topk)     # no slot past the row is ever kept
     return kept
+
+
+def _chunked_compaction(key: np.ndarray, n: int, K: int, whole: bool, need_eq: int, topk: int,
+                        chunk: int) -> np.ndarray:
+    """The long-row compaction: chunks in pool order, each ranking its kept pools after the running
+    count of kept pools and deciding its ties after the running count of ties; stops at topk."""
+    out = np.full(topk, -1, np.int64)
+    sel_base = eq_base = 0
+    for c0 in range(0, len(key), chunk):
+        if sel_base >= topk:
+            break
+        kc = key[c0:c0 + chunk]
+        gt = kc >= K if whole else kc > K
+        eq = np.zeros_like(gt) if whole else kc == K
+        take = gt | eq
+        eq_idx = np.flatnonzero(eq)
+        take[eq_idx[eq_base + np.arange(len(eq_idx)) >= need_eq]] = False
+        eq_base += len(eq_idx)
+        kept = np.flatnonzero(take)
+        rank = sel_base + np.arange(len(kept))
+        ok = rank < topk
+        out[rank[ok]] = c0 + kept[ok]
+        sel_base += len(kept)
+    assert np.all(out >= 0) and np.all(out < n)
+    return out
+
+
+def _threshold(key: np.ndarray, topk: int) -> tuple[int, bool, int]:
+    """(K, whole, need_eq) of the three radix levels, as the kernel finds them: a level's bin is kept
+    whole when its count is exactly the number of keys still needed."""
+    levels = ((0x00000000, 21, 2048), (0xFFE00000, 10, 2048), (0xFFFFFC00, 0, 1024))
+    prefix, rem = 0, topk
+    for hi_mask, shift, nbins in levels:
+        inbin = (key & hi_mask) == prefix
+        hist = np.bincount(((key[inbin] >> shift) & (nbins - 1)).astype(np.int64), minlength=nbins)
+        d, rem = _pick(hist, rem)
+        prefix |= d << shift
+        if int(hist[d]) == rem and shift > 0:
+            return prefix, True, 0
+    return prefix, False, rem
 
 
 def _rows(kind: str, n: int, rng) -> np.ndarray:
@@ -101,3 +131,20 @@ def test_key_order_matches_the_oracle_order():
     k = _keys(s)
     assert k[0] == 0 and np.all(np.diff(k[1:].astype(np.int64)) >= 0)
     assert k[5] == k[6] and np.all(np.diff(np.delete(k[1:], 4).astype(np.int64)) > 0)
+
+
+@pytest.mark.parametrize("kind", ["normal", "few_values", "all_equal", "mostly_nan", "tiny_and_huge"])
+@pytest.mark.parametrize("chunk", [256, 1024, 8192])
+def test_chunked_compaction_keeps_the_oracle_pools(kind, chunk):
+    """Rows of several chunks (chunk sizes scaled down from the kernel's 8192 so that small rows span
+    many): carrying the kept and tied counts from chunk to chunk keeps the oracle's pools."""
+    rng = np.random.default_rng([chunk, len(kind), 7])
+    topk = 64
+    for n in (300, 2049, 9000):
+        s = _rows(kind, n, rng)
+        n_pad = -(-n // 256) * 256
+        key = np.zeros(n_pad, np.uint64)
+        key[:n] = _keys(s)
+        K, whole, need_eq = _threshold(key, topk)
+        got = _chunked_compaction(key, n, K, whole, need_eq, topk, chunk)
+        np.testing.assert_array_equal(got, O.select_pools(s, topk))
