@@ -251,8 +251,11 @@ int kpool_forward_host(const kpool_host_io* host, const kpool_dev_io* dev, int32
  * Limits: layout->T <= 4096, layout->n_docs <= 256, n_idx_heads * d_idx <=
  * 4096; larger sizes return KPOOL_ERR_SHAPE before any launch.
  * The first call on each device looks up the array's device address
- * (cudaGetSymbolAddress); make that first call before any stream capture
- * begins.  Every call uses the same array and leaves its contents behind
+ * (cudaGetSymbolAddress) and keeps it for the rest of the process; make that
+ * first call before any stream capture begins.  The kept address does not
+ * survive a teardown of the device's context (cudaDeviceReset): after one,
+ * the array may sit elsewhere, so do not call this entry point on that
+ * device again in the same process.  Every call uses the same array and leaves its contents behind
  * (each call writes every scratch byte it later reads, so nothing needs to
  * start at zero); calls that can overlap on the GPU (different streams, or
  * other threads) race on the array and must be serialised by the caller.
@@ -364,6 +367,26 @@ int dsa_decode_index(const void* q_idx, const float* w, const uint8_t* k8_cache,
  *   row_ids  int32 [n_ids], device; ids outside [0, rows) are skipped */
 int kpool_measure_l2_reduce(float* buf, int32_t rows, const int32_t* row_ids, int32_t n_ids,
                             kpool_stream_t stream);
+
+/* kpool_debug_inject_stall: test utility, no counterpart on the pages.
+ * Every wait of the tcgen05 kernels on an mbarrier is bounded: after about
+ * two seconds it records KPOOL_ERR_TIMEOUT in the call's status word, every
+ * warp role leaves its loop, copies and MMAs in flight are waited for and
+ * TMEM is freed, so the context stays usable.  This hook makes that path run
+ * on demand: with KPOOL_STALL_SCORE set, every later launch of the tcgen05
+ * scoring kernel (dsa_index with d_idx = 128) first waits on a barrier that
+ * nothing completes, in its MMA issuer; with KPOOL_STALL_SPARSE_MLA, every
+ * later sparse_mla_fwd / sparse_mla_fwd_rows launch does the same in its PV
+ * issuer.  Such a launch takes about two seconds, ends with
+ * KPOOL_ERR_TIMEOUT and leaves its outputs undefined.  mask = 0 restores
+ * normal operation (the state at load).  The setting is per device (the
+ * current one) and applies to launches enqueued after the call returns; it
+ * synchronises with the device like cudaMemcpyToSymbol.
+ * Returns KPOOL_ERR_INVALID_ARG for unknown bits, KPOOL_ERR_CUDA if the copy
+ * fails. */
+#define KPOOL_STALL_SCORE 1
+#define KPOOL_STALL_SPARSE_MLA 2
+int kpool_debug_inject_stall(int32_t mask);
 
 /* kpool_cast_e4m3: test and diagnostic utility, no counterpart on the pages.
  * codes[k] = OCP E4M3 ("fn") code of x[k], k < n: round to nearest, ties to

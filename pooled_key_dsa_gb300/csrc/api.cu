@@ -166,6 +166,13 @@ int kpool_cast_e4m3(const float* x, int64_t n, uint8_t* codes, kpool_stream_t st
     return launch_cast_e4m3(x, n, codes, reinterpret_cast<cudaStream_t>(stream));
 }
 
+int kpool_debug_inject_stall(int32_t mask) {
+    if (mask & ~(KPOOL_STALL_SCORE | KPOOL_STALL_SPARSE_MLA)) return KPOOL_ERR_INVALID_ARG;
+    int rc = set_score_tc_stall(mask & KPOOL_STALL_SCORE);
+    if (rc == KPOOL_OK) rc = set_sparse_mla_stall(mask & KPOOL_STALL_SPARSE_MLA);
+    return rc;
+}
+
 int kpool_measure_l2_reduce(float* buf, int32_t rows, const int32_t* row_ids, int32_t n_ids,
                             kpool_stream_t stream) {
     if (rows < 0 || n_ids < 0) return KPOOL_ERR_SHAPE;

@@ -60,6 +60,11 @@ int launch_sparse_mla_bwd(const uint16_t* q_lat, const uint16_t* kv_lat, const i
                           const uint16_t* dout, uint16_t* dq, float* dkv, float* delta, int32_t* status,
                           cudaStream_t stream);
 
+// Test hooks of the bounded waits: nonzero makes the next launches of the kernel wait first on a barrier
+// that is never completed (tcgen05 scoring: its MMA issuer; sparse MLA: its PV issuer).
+int set_score_tc_stall(int on);
+int set_sparse_mla_stall(int on);
+
 // Measurement: fp32 reductions into 512-float rows (the dKv scatter's access pattern).
 int launch_l2_reduce(float* buf, int rows, const int32_t* row_ids, int n_ids, cudaStream_t stream);
 

@@ -52,7 +52,9 @@ std::mutex g_mu;
 void* g_scratch_ptr[MAX_DEVICES] = {nullptr};
 
 // Device address of the scratch on the current device, looked up once per
-// device (the lookup loads this file's device code on that device).
+// device (the lookup loads this file's device code on that device) and kept
+// for the process.  A reset of the device's context can move the array, so
+// the kept address is valid only until such a reset.
 int scratch_on_current_device(void** out) {
     int dev = -1;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEVICES) return KPOOL_ERR_CUDA;

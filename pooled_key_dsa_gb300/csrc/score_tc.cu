@@ -46,6 +46,7 @@ constexpr int OFF_SMALL = OFF_WS + 4 * 256 * 4;     // two groups x two items x 
 
 struct ScSmall {
     uint64_t b_full[2], b_empty[2], a_full[A_STAGES], a_empty[A_STAGES], acc_full[2], acc_empty[2], drain;
+    uint64_t never;                    // no thread arrives on it: the stall hook waits here
     int abort;
     uint32_t tmem;
 };
@@ -135,7 +136,16 @@ __device__ __forceinline__ void score_chunk(const uint32_t (&v)[32], const float
     }
 }
 
+// Nonzero: the next launches stall their MMA issuer on a barrier that is never
+// completed (test of the bounded waits; set with set_score_tc_stall).
+__device__ int g_score_tc_stall = 0;
+
 }  // namespace
+
+int set_score_tc_stall(int on) {
+    const int v = on ? 1 : 0;
+    return cudaMemcpyToSymbol(g_score_tc_stall, &v, sizeof(v)) == cudaSuccess ? KPOOL_OK : KPOOL_ERR_CUDA;
+}
 
 template <int HI>
 __global__ void __launch_bounds__(SC_THREADS, 1) score_tc_kernel(
@@ -164,6 +174,7 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_tc_kernel(
             tc::mbar_init(tc::smem_u32(&sm.a_empty[s]), 1);
         }
         tc::mbar_init(tc::smem_u32(&sm.drain), 1);
+        tc::mbar_init(tc::smem_u32(&sm.never), 1);
         sm.abort = 0;
         tc::mbar_init_fence();
     }
@@ -202,13 +213,26 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_tc_kernel(
                 sm.abort = 1;
                 set_status(status, KPOOL_ERR_TIMEOUT);
             }
+            // no TMA load may still be writing shared memory when the CTA ends: wait (bounded by the
+            // full limit, whatever the outcome) for the last load issued into every buffer.  The
+            // parity is that of the load's own phase; the barrier cannot have moved past it, since
+            // no later load went into the same buffer.
+            for (int s = 0; s < A_STAGES; ++s) {
+                if ((uint32_t)s >= na) break;
+                const uint32_t last = na - 1 - ((na - 1 - (uint32_t)s) % A_STAGES);   // last load into stage s
+                tc::mbar_wait_for(tc::smem_u32(&sm.a_full[s]), (last / A_STAGES) & 1, tc::WAIT_LIMIT_NS);
+            }
+            for (uint32_t n = ni >= 2 ? ni - 2 : 0; n < ni; ++n)
+                tc::mbar_wait_for(tc::smem_u32(&sm.b_full[n & 1]), (n >> 1) & 1, tc::WAIT_LIMIT_NS);
         }
         __syncwarp();
     } else if (warp == 1) {
         // ===================================================== MMA issuer
         if (lane == 0) {
             uint32_t ni = 0, na = 0, nacc = 0;
-            bool ok = true;
+            // test hook: with a stall injected, wait first on a barrier that nothing completes, so the
+            // bounded wait runs out while the TMA producer has filled the ring
+            bool ok = g_score_tc_stall == 0 || tc::mbar_wait(tc::smem_u32(&sm.never), 0, abort_flag);
             for (int k = 0; ok && !*abort_flag; ++k, ++ni) {
                 const int j = item_of(k);
                 if (j >= total) break;

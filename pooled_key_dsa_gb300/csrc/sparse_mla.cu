@@ -92,6 +92,7 @@ constexpr int OFF_SMALL = OFF_P + NSB * P_BYTES;
 
 struct Small {
     uint64_t q_full, q_empty, o_full, o_free, drain;
+    uint64_t never;                             // no thread arrives on it: the stall hook waits here
     uint64_t kv_full[NSTAGE], kv_empty[NSTAGE];
     uint64_t s_full[NSB], s_free[NSB], p_full[NSB], p_empty[NSB], o_step[NSB];
     uint64_t nb_full[2], nb_empty[2];           // row-scan results, two queries deep
@@ -159,7 +160,16 @@ __device__ __forceinline__ bool warp_wait(uint32_t addr, uint32_t parity, const 
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
+// Nonzero: the next launches stall their PV issuer on a barrier that is never
+// completed (test of the bounded waits; set with set_sparse_mla_stall).
+__device__ int g_sparse_mla_stall = 0;
+
 }  // namespace
+
+int set_sparse_mla_stall(int on) {
+    const int v = on ? 1 : 0;
+    return cudaMemcpyToSymbol(g_sparse_mla_stall, &v, sizeof(v)) == cudaSuccess ? KPOOL_OK : KPOOL_ERR_CUDA;
+}
 
 template <bool ONE_QUERY>
 __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_t* __restrict__ q_lat,
@@ -181,6 +191,7 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
         tc::mbar_init(tc::smem_u32(&sm.o_full), 1);
         tc::mbar_init(tc::smem_u32(&sm.o_free), 4);
         tc::mbar_init(tc::smem_u32(&sm.drain), 3);
+        tc::mbar_init(tc::smem_u32(&sm.never), 1);
         for (int r = 0; r < 2; ++r) {
             tc::mbar_init(tc::smem_u32(&sm.nb_full[r]), 1);        // the row scanner
             tc::mbar_init(tc::smem_u32(&sm.nb_empty[r]), NGATH);   // every gather warp has read it
@@ -353,7 +364,9 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
         // ===================================================== PV issuer
         if (lane == 0) {
             uint32_t g = 0, qn = 0;
-            bool ok = true;
+            // test hook: with a stall injected, wait first on a barrier that nothing completes, so the
+            // bounded wait runs out while the producers, S issuers and softmax warps are mid-stream
+            bool ok = g_sparse_mla_stall == 0 || tc::mbar_wait(tc::smem_u32(&sm.never), 0, abort_flag);
             for (int i = blockIdx.x; i < n_rows && ok && !*abort_flag; i += gridDim.x, ++qn) {
                 if (!tc::mbar_wait(tc::smem_u32(&sm.q_full), qn & 1, abort_flag)) { ok = false; break; }
                 const int nb = sm.nb;

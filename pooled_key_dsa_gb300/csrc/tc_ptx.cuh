@@ -161,6 +161,14 @@ __device__ __forceinline__ bool mbar_wait(uint32_t addr, uint32_t parity, const 
     }
 }
 
+// Bounded wait with its own limit and no abort flag (the end-of-kernel drains).
+__device__ __forceinline__ bool mbar_wait_for(uint32_t addr, uint32_t parity, uint64_t limit_ns) {
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try(addr, parity))
+        if (globaltimer_ns() - t0 > limit_ns) return false;
+    return true;
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t addr, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;\n" ::"r"(addr), "r"(bytes)
                  : "memory");

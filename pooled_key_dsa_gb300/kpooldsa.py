@@ -24,7 +24,8 @@ EXPORTED = ("kpool_workspace_bytes", "kpool_workspace_offsets", "kpool_build", "
             "kpool_stage_select", "kpool_set_stage_events", "kpool_check_status", "kpool_strerror", "kpool_version",
             "dsa_index_noalloc", "sparse_mla_fwd_rows", "kpool_forward_host", "mla_absorb_q", "mla_v_proj",
             "sparse_mla_bwd", "kpool_measure_l2_reduce", "kpool_paged_append", "dsa_decode_workspace_bytes",
-            "dsa_decode_index", "kpool_cast_e4m3")
+            "dsa_decode_index", "kpool_cast_e4m3", "kpool_debug_inject_stall")
+STALL_SCORE, STALL_SPARSE_MLA = 1, 2
 
 
 class KpoolUnavailable(ImportError):
@@ -92,6 +93,7 @@ def lib():
         L.sparse_mla_bwd.argtypes = [vp, vp, vp, i32, i32, i32, ctypes.c_float, vp, vp, vp, vp, vp, vp, vp, vp]
         L.kpool_measure_l2_reduce.argtypes = [vp, i32, vp, i32, vp]
         L.kpool_cast_e4m3.argtypes = [vp, ctypes.c_int64, vp, vp]
+        L.kpool_debug_inject_stall.argtypes = [i32]
         L.kpool_paged_append.argtypes = [vp, vp, vp, vp, vp, vp, i32, vp, i32, i32, ctypes.POINTER(Params), vp, vp,
                                          vp, vp]
         L.dsa_decode_workspace_bytes.argtypes = [ctypes.POINTER(Params), i32, i32]
@@ -315,6 +317,13 @@ def measure_l2_reduce(buf, row_ids, stream=None):
         raise ValueError("buf must be [rows, 512]")
     _check(lib().kpool_measure_l2_reduce(_ptr(buf), buf.shape[0], _ptr(row_ids), row_ids.numel(), _stream(stream)),
            "kpool_measure_l2_reduce")
+
+
+def debug_inject_stall(mask: int) -> None:
+    """Test hook of the bounded waits: STALL_SCORE / STALL_SPARSE_MLA make the later launches of the tcgen05
+    scoring / sparse attention kernels wait first on a barrier that nothing completes, so that they end with
+    KPOOL_ERR_TIMEOUT after the wait limit; 0 restores normal operation."""
+    _check(lib().kpool_debug_inject_stall(int(mask)), "kpool_debug_inject_stall")
 
 
 def cast_e4m3(x, out=None, stream=None):

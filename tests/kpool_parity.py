@@ -8,6 +8,7 @@ import torch
 from oracle import kpool_oracle as O
 from pooled_key_dsa_gb300 import kpooldsa as K
 from pooled_key_dsa_gb300 import workloads
+from tests import oracle_rows as OR
 
 # Tolerances (floating point): pooled keys within 1e-5 of the magnitude of the
 # keys they mix; attention output 2e-2 max / 5e-3 mean absolute; LSE 1e-3
@@ -17,7 +18,7 @@ KPOOL_RTOL = 1e-5
 OUT_MAX_ABS = 2e-2
 OUT_MEAN_ABS = 5e-3
 LSE_ABS = 1e-3
-BOUNDARY_RTOL = 1e-3
+BOUNDARY_RTOL = OR.BOUNDARY_RTOL
 
 
 def params_of(wl: workloads.Workload) -> K.Params:
@@ -86,51 +87,28 @@ def gpu_row_scores(res, layout, i):
     return res["scores_raw"][start:start + n_i]
 
 
-def compare_rows(gpu_rows, layout, rows, oracle_scores, topk, W):
-    """Compares GPU index rows with the oracle's selection rule.  Returns a
-    dict of counts; 'hard' counts rows that differ other than at boundary
-    pools (pools whose oracle score is within BOUNDARY_RTOL of the row's
-    topk-th score)."""
-    stats = {"rows": 0, "exact": 0, "boundary_rows": 0, "boundary_pools": 0, "hard": 0, "hard_rows": []}
-    for n, i in enumerate(rows):
-        i = int(i)
-        d, r, n_i, tail = O.query_geometry(layout, i)
-        S = oracle_scores[n]
-        sel = O.select_pools(S, topk)
-        want = O.index_row(layout, i, sel, W)
-        got = gpu_rows[n]
-        stats["rows"] += 1
-        if np.array_equal(got, want):
-            stats["exact"] += 1
-            continue
-        # structural validity of the GPU row
-        valid = got[got >= 0]
-        nv = 4 * min(topk, n_i) + tail
-        s_d = int(layout["cu_seqlens"][d])
-        ok = (len(valid) == nv and np.all(got[nv:] == -1) and np.all(np.diff(valid) > 0)
-              and valid.min() >= s_d and valid.max() <= i)
-        if ok and tail:
-            ok = valid[-tail:].tolist() == list(range(i - tail + 1, i + 1))
-        gsel = np.zeros(0, np.int64)
-        if ok:
-            blocks = (valid[:nv - tail] - s_d).reshape(-1, 4)
-            ok = bool(np.all(blocks == blocks[:, :1] + np.arange(4)) and np.all(blocks[:, 0] % 4 == 0))
-            gsel = blocks[:, 0] // 4
-        if not ok:
-            stats["hard"] += 1
-            stats["hard_rows"].append(i)
-            continue
-        Sd = np.asarray(S, np.float64)
-        kth = np.sort(Sd)[::-1][min(topk, n_i) - 1]
-        diff = set(gsel.tolist()) ^ set(sel.tolist())
-        near = all(abs(Sd[p] - kth) <= BOUNDARY_RTOL * abs(kth) for p in diff)
-        if near:
-            stats["boundary_rows"] += 1
-            stats["boundary_pools"] += len(diff) // 2
-        else:
-            stats["hard"] += 1
-            stats["hard_rows"].append(i)
-    return stats
+compare_rows = OR.compare_rows
+
+# One summary line per parity check of the index rows (rows, bit-exact, boundary rows and pools, hard), printed
+# again at the end of the pytest run so that the counts reach the run's record even under -q.
+PARITY_LOG = []
+
+
+def record(line: str) -> None:
+    PARITY_LOG.append(line)
+    print(line)
+
+
+def check_index_rows(wl, res, inp, lay_o, rows, workers=None):
+    """Oracle check of the given query rows of the GPU indexer, in parallel over rows: the query FP8 codes and
+    head weights bit-exact, the scores within 1e-5 of each row's largest, the index rows by the selection rule
+    (bit-exact up to counted boundary pools).  Returns the merged counts."""
+    rows = np.asarray(rows, np.int64)
+    qbits = inp.q_idx.view(torch.int16).numpy().view(np.uint16)
+    scores = [gpu_row_scores(res, lay_o, int(i)) for i in rows]
+    shared = {"k8": res["k8"], "s_k": res["s_k"], "w": inp.w, "layout": lay_o, "topk": res["topk"], "W": res["W"]}
+    return OR.check_rows(rows, qbits[rows], res["q8"][rows], res["ws"][rows], scores, res["indices"][rows], shared,
+                         workers=workers)
 
 
 def attention_check(out_gpu, lse_gpu, out_ref, lse_ref):

@@ -128,6 +128,12 @@ def test_host_checks_of_the_projection_entries(lib):
         assert fn(None, None, 0, 64, 128, 128, None, None, None) == K.KPOOL_OK        # T = 0: nothing to do
 
 
+def test_host_checks_of_the_stall_hook(lib):
+    """Unknown bits of the stall mask are rejected before any device call."""
+    assert lib.kpool_debug_inject_stall(4) == K.CODES["KPOOL_ERR_INVALID_ARG"]
+    assert lib.kpool_debug_inject_stall(-1) == K.CODES["KPOOL_ERR_INVALID_ARG"]
+
+
 def test_host_checks_of_the_cast_entry(lib):
     vp = ctypes.c_void_p
     cast = lib.kpool_cast_e4m3

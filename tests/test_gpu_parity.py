@@ -59,35 +59,21 @@ def _parity_of(wl, rows=None, attn_rows=None, attention=True):
     k8_e2e, _ = O.quantize_keys(kp_o)
     assert np.array_equal(res["k8"][:lay_o["n_pools"]], k8_e2e)
 
-    rows = np.arange(wl.T) if rows is None else rows
-    qf = inp.q_idx.float().numpy()
-    q8_o, sq_o = O.quantize_queries(qf[rows])
-    np.testing.assert_array_equal(res["q8"][rows], q8_o)
-    ws_o = (inp.w[rows] * sq_o).astype(np.float32)
-    np.testing.assert_array_equal(res["ws"][rows].view(np.uint32), ws_o.view(np.uint32))
-
-    # scores of the scored rows (fp32 accumulation order differs from fp64)
-    S_o = O.scores_fp8(q8_o, sq_o, res["k8"], res["s_k"], inp.w, lay_o, rows)
-    worst = 0.0
-    for n, i in enumerate(rows):
-        g = KP.gpu_row_scores(res, lay_o, int(i))
-        if g is None:
-            continue
-        o = S_o[n].astype(np.float64)
-        scale = max(np.abs(o).max(), 1e-30)
-        worst = max(worst, float(np.abs(g - o).max() / scale))
-    assert worst <= 1e-5, worst
-
-    stats = KP.compare_rows(res["indices"][rows], lay_o, rows, S_o, wl.topk, res["W"])
-    print(f"\n[{wl.name}] index rows: {stats['exact']}/{stats['rows']} bit-exact, "
-          f"{stats['boundary_rows']} boundary rows ({stats['boundary_pools']} pools), hard {stats['hard']}; "
-          f"score rel err {worst:.2e}")
-    assert stats["hard"] == 0, stats["hard_rows"][:10]
+    rows = np.arange(wl.T) if rows is None else np.asarray(rows, np.int64)
+    chk = KP.check_index_rows(wl, res, inp, lay_o, rows)
+    st = chk["stats"]
+    KP.record(f"[{wl.name}] index rows: {st['rows']} checked ({'all' if len(rows) == wl.T else 'sample'} of "
+              f"{wl.T}), {st['exact']} bit-exact, {st['boundary_rows']} boundary rows ({st['boundary_pools']} "
+              f"pools), hard {st['hard']}; q8 rows off {chk['q8_bad']}, ws rows off {chk['ws_bad']}; "
+              f"score rel err {chk['worst']:.2e}")
+    assert chk["q8_bad"] == 0 and chk["ws_bad"] == 0
+    assert chk["worst"] <= 1e-5, chk["worst"]
+    assert st["hard"] == 0, st["hard_rows"][:10]
     if not attention:
         return wl, res
 
     # attention, evaluated by the oracle on the GPU's own index rows
-    attn_rows = rows if attn_rows is None else attn_rows
+    attn_rows = rows if attn_rows is None else np.asarray(attn_rows, np.int64)
     ql = workloads.q_lat(wl)
     out, lse = K.sparse_mla_fwd(ql.cuda(), dev["kv_lat"], res["indices_dev"], wl.scale)
     torch.cuda.synchronize()
@@ -96,7 +82,7 @@ def _parity_of(wl, rows=None, attn_rows=None, attention=True):
     out_o, lse_o = O.sparse_attention(ql[torch.from_numpy(attn_rows)].float().numpy(), inp.kv_lat.float().numpy(),
                                       res["indices"][attn_rows], wl.scale, attn_rows)
     mx, mean, le = KP.attention_check(out_g, lse_g, out_o, lse_o)
-    print(f"[{wl.name}] attention: max abs {mx:.3e}, mean abs {mean:.3e}, lse {le:.3e}")
+    KP.record(f"[{wl.name}] attention ({len(attn_rows)} rows): max abs {mx:.3e}, mean abs {mean:.3e}, lse {le:.3e}")
     assert mx <= KP.OUT_MAX_ABS and mean <= KP.OUT_MEAN_ABS and le <= KP.LSE_ABS
     return wl, res
 
@@ -114,24 +100,33 @@ def test_parity_tiny_workload():
 
 
 def test_parity_single_doc_4096_cutover():
+    """Every index row; attention on the seeded sample."""
     wl = workloads.workload(1)
-    _full_parity(1, rows=KP.sample_rows(wl, n_uniform=400, seed=1))
+    _full_parity(1, rows=None, attn_rows=KP.sample_rows(wl, n_uniform=400, seed=1))
 
 
 def test_parity_packed_8192_six_docs():
+    """Every index row; attention on the seeded sample."""
     wl = workloads.workload(2)
-    _full_parity(2, rows=KP.sample_rows(wl, n_uniform=400, seed=2))
+    _full_parity(2, rows=None, attn_rows=KP.sample_rows(wl, n_uniform=400, seed=2))
 
 
 def test_parity_headline_32768():
+    """Every index row; attention on the seeded sample."""
     wl = workloads.workload(3)
-    _full_parity(3, rows=KP.sample_rows(wl, n_uniform=256, seed=3))
+    _full_parity(3, rows=None, attn_rows=KP.sample_rows(wl, n_uniform=256, seed=3))
 
 
 @pytest.mark.slow
 def test_parity_long_131072():
+    """Several thousand index rows (the seeded sample, the last 64 rows of every document and 4096 uniform
+    rows); attention on the seeded sample."""
     wl = workloads.workload(4)
-    _full_parity(4, rows=KP.sample_rows(wl, n_uniform=192, seed=4))
+    sample = KP.sample_rows(wl, n_uniform=192, seed=4)
+    extra = [np.arange(max(s, e - 64), e) for s, e in zip(wl.cu_seqlens[:-1], wl.cu_seqlens[1:])]
+    uni = np.random.default_rng(44).integers(0, wl.T, 4096)
+    rows = np.unique(np.concatenate([sample, uni, *extra]))
+    _full_parity(4, rows=rows, attn_rows=sample)
 
 
 # ----------------------------------------------------------------- stage isolation

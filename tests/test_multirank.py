@@ -78,7 +78,7 @@ def test_layer_roofline_fraction_of_the_step():
     from pooled_key_dsa_gb300 import workloads
     wl = workloads.workload(3)
     work = bench._work(wl)
-    peaks = {"hbm_gbs": 6000.0, "bf16_sustained": 1700.0, "source": "test"}
+    peaks = {"hbm_gbs": 6000.0, "bf16": 1700.0, "bf16_sustained": 1500.0, "source": "test"}
     first = bench.layer_roofline(wl, work, {k: 1.0 for k in ("kpool_build", "hadamard_fp8", "score", "select",
                                                               "sparse_mla")}, peaks, 3400.0)
     r = first["t_roof_ms"]
