@@ -18,8 +18,8 @@
 // so the epilogues of consecutive tiles run side by side.  A thread owns one
 // pool (its TMEM lane) and all 256 columns, read in 32-column loads issued one
 // chunk ahead; ReLU, the head weights and the head sum stay thread-local
-// (packed fp32 FMAs, independent partial sums); one coalesced store per
-// (query, pool).
+// (packed fp32 adds and FMAs, independent partial sums); one coalesced store
+// per (query, pool).
 // Items are spread over the persistent CTAs in a snake order (the item size
 // grows along a document).  Waits are bounded (KPOOL_ERR_TIMEOUT).
 #include <cstdint>
@@ -121,7 +121,11 @@ __device__ __forceinline__ void score_chunk(const uint32_t (&v)[32], const float
             const int c = qq * HC + 2 * jp;           // column within the chunk
             const float4 wv = w4[c >> 2];
             const float2 w2 = (c & 2) ? make_float2(wv.z, wv.w) : make_float2(wv.x, wv.y);
-            const float2 x = make_float2(fmaxf(__uint_as_float(v[c]), 0.f), fmaxf(__uint_as_float(v[c + 1]), 0.f));
+            // 2*ReLU(a) = a + |a|, exact (+0 for a <= 0; the accumulator is never NaN), as one packed
+            // add on the FMA pipe instead of a max per element on the ALU pipe; the head weights in
+            // shared memory carry the factor 1/2 (exact for normal values), so each product is ws * ReLU(a)
+            const float a0 = __uint_as_float(v[c]), a1 = __uint_as_float(v[c + 1]);
+            const float2 x = __fadd2_rn(make_float2(a0, a1), make_float2(fabsf(a0), fabsf(a1)));
             if (jp < NP)
                 part[jp] = __fmul2_rn(x, w2);
             else
@@ -188,7 +192,9 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_tc_kernel(
         // ===================================================== TMA producer
         if (lane == 0) {
             uint32_t ni = 0, na = 0;
-            bool ok = true;
+            // test hook: with a stall injected, wait first on a barrier that nothing completes, so the
+            // bounded waits of every role run out
+            bool ok = g_score_tc_stall == 0 || tc::mbar_wait(tc::smem_u32(&sm.never), 0, abort_flag);
             for (int k = 0; ok; ++k, ++ni) {
                 const int j = item_of(k);
                 if (j >= total) break;
@@ -230,9 +236,7 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_tc_kernel(
         // ===================================================== MMA issuer
         if (lane == 0) {
             uint32_t ni = 0, na = 0, nacc = 0;
-            // test hook: with a stall injected, wait first on a barrier that nothing completes, so the
-            // bounded wait runs out while the TMA producer has filled the ring
-            bool ok = g_score_tc_stall == 0 || tc::mbar_wait(tc::smem_u32(&sm.never), 0, abort_flag);
+            bool ok = true;
             for (int k = 0; ok && !*abort_flag; ++k, ++ni) {
                 const int j = item_of(k);
                 if (j >= total) break;
@@ -284,10 +288,10 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_tc_kernel(
             if (j >= total) break;
             const Item it = decode_item(j, sched, cu_seqlens, cu_pools, n_docs, topk, QG);
             const int i0 = it.s_d + it.r0;
-            // the item's head weights (256 floats) into this group's shared buffer
+            // the item's head weights (256 floats), halved, into this group's shared buffer
             float* wsb = reinterpret_cast<float*>(smem + OFF_WS) + g * 512 + (ni & 1) * 256;
-            wsb[e] = (it.r0 + e / HI < it.L) ? ws[(int64_t)i0 * HI + e] : 0.f;
-            wsb[e + 128] = (it.r0 + (e + 128) / HI < it.L) ? ws[(int64_t)i0 * HI + e + 128] : 0.f;
+            wsb[e] = (it.r0 + e / HI < it.L) ? 0.5f * ws[(int64_t)i0 * HI + e] : 0.f;
+            wsb[e + 128] = (it.r0 + (e + 128) / HI < it.L) ? 0.5f * ws[(int64_t)i0 * HI + e + 128] : 0.f;
             if (group_or(bad, g)) { bad = true; break; }
             const int64_t row_base = pair_base[it.d];
             // per query: the start of its score row and its pool count (0: no scored row)

@@ -42,9 +42,13 @@
 //   warps 4-7  softmax: lane l < 16 loads the K-half-0 row of head 16w+l and
 //              lane l+16 the K-half-1 row; a half-row exchange between the two
 //              leaves lane l with slots 0-31 and lane l+16 with slots 32-63 of
-//              the summed row.  The running max only moves (and O^T is
-//              rescaled) when a slot beats it by more than 2^8; a vote on that
-//              is the only barrier of a block in the common case.  When every
+//              the summed row.  The running max only moves when a slot beats it
+//              by more than 2^8; each warp decides that for its own heads, with
+//              no barrier between the four.  A move of a max that O^T already
+//              depends on raises a flag that the PV issuer reads with the P^T
+//              tile: it then asks the four warps (served inside their waits) to
+//              rescale O^T after the previous PV and only then issues this one.
+//              When every
 //              slot of the warp's half-blocks is valid (all but a row's last
 //              block), the test runs on the unscaled block max and the scale is
 //              fused into the exponent's FMA.  P^T goes to
@@ -60,7 +64,7 @@
 //              ONE_QUERY instance reads the row with 16-byte loads)
 // Every wait is bounded and warp-uniform (lane 0 polls, the warp takes its
 // answer); on expiry the kernel records KPOOL_ERR_TIMEOUT, the softmax warps
-// agree on stopping at their next named barrier, every role leaves its loop,
+// agree on stopping at the next query-level named barrier, every role leaves its loop,
 // in-flight copies and MMAs are drained and TMEM is freed.
 #include <cstdint>
 
@@ -92,7 +96,6 @@ constexpr int OFF_SMALL = OFF_P + NSB * P_BYTES;
 
 struct Small {
     uint64_t q_full, q_empty, o_full, o_free, drain;
-    uint64_t never;                             // no thread arrives on it: the stall hook waits here
     uint64_t kv_full[NSTAGE], kv_empty[NSTAGE];
     uint64_t s_full[NSB], s_free[NSB], p_full[NSB], p_empty[NSB], o_step[NSB];
     uint64_t nb_full[2], nb_empty[2];           // row-scan results, two queries deep
@@ -102,6 +105,11 @@ struct Small {
     int abort;
     uint32_t tmem;
     float alpha[2][HP];
+    uint64_t resc_done;                         // the softmax warps have rescaled O^T for a request
+    uint8_t resc_flag[NSB][4];                  // per P buffer: softmax warp w raised a head's max
+    uint32_t resc_mask;                         // flags of the outstanding request
+    int resc_g;                                 // block of the outstanding request
+    int resc_seq;                               // requests issued so far
     alignas(16) float inv_l[HP];
 };
 constexpr int SMEM_BYTES = OFF_SMALL + (int)sizeof(Small) + 1024;   // + alignment slack
@@ -146,6 +154,15 @@ __device__ __forceinline__ bool wg_or(bool pred) {
     return r != 0;
 }
 
+__device__ __forceinline__ int ld_acquire(const int* p) {
+    int v;
+    asm volatile("ld.acquire.cta.shared::cta.b32 %0, [%1];\n" : "=r"(v) : "r"(tc::smem_u32(p)) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release(int* p, int v) {
+    asm volatile("st.release.cta.shared::cta.b32 [%0], %1;\n" ::"r"(tc::smem_u32(p)), "r"(v) : "memory");
+}
+
 // Per-warpgroup register budgets (launch: 512 threads x 128).  Shares: the two
 // producer warpgroups 104 each, softmax 168, issuers and row scanner 80 (sum 456).
 template <uint32_t N>
@@ -160,9 +177,42 @@ __device__ __forceinline__ bool warp_wait(uint32_t addr, uint32_t parity, const 
     return __shfl_sync(0xffffffffu, ok, 0) != 0;
 }
 
-// Nonzero: the next launches stall their PV issuer on a barrier that is never
-// completed (test of the bounded waits; set with set_sparse_mla_stall).
+// Nonzero: the next launches stall their row scanner on a barrier that cannot
+// complete before the kernel aborts (test of the bounded waits; set with
+// set_sparse_mla_stall).
 __device__ int g_sparse_mla_stall = 0;
+
+// A rescale request of the PV issuer: multiply the O^T columns of the heads whose running max moved
+// (the flagged warps' heads; the others by 1) by their factors, once the previous block's PV has landed.
+// Every softmax warp serves it on its 32 lanes (tm = the warp's TMEM lane base); the PV issuer waits
+// for all four.
+__device__ __forceinline__ bool serve_rescale(Small& sm, uint32_t tm, const volatile int* abort_flag) {
+    const int gr = *reinterpret_cast<volatile int*>(&sm.resc_g);
+    const uint32_t fm = *reinterpret_cast<volatile uint32_t*>(&sm.resc_mask);
+    const uint32_t gp = (uint32_t)gr - 1u;
+    if (!warp_wait(tc::smem_u32(&sm.o_step[gp % NSB]), (gp / NSB) & 1, abort_flag)) return false;
+    tc::fence_after();
+    const float* al = sm.alpha[gr % NSB];
+    for (int t = 0; t < 4; ++t)
+        for (int c0 = 0; c0 < HP; c0 += 32) {
+            uint32_t o[32];
+            const uint32_t ta = tm + TM_O + 64 * t + c0;
+            tc::tmem_ld32(ta, o);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const int c = c0 + j;
+                const float f = ((fm >> (8 * (c >> 4))) & 1u) ? al[c] : 1.f;
+                o[j] = __float_as_uint(__uint_as_float(o[j]) * f);
+            }
+            tc::tmem_st32(ta, o);
+        }
+    tc::tmem_wait_st();
+    tc::fence_before();
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) tc::mbar_arrive(tc::smem_u32(&sm.resc_done));
+    return true;
+}
 
 }  // namespace
 
@@ -191,7 +241,6 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
         tc::mbar_init(tc::smem_u32(&sm.o_full), 1);
         tc::mbar_init(tc::smem_u32(&sm.o_free), 4);
         tc::mbar_init(tc::smem_u32(&sm.drain), 3);
-        tc::mbar_init(tc::smem_u32(&sm.never), 1);
         for (int r = 0; r < 2; ++r) {
             tc::mbar_init(tc::smem_u32(&sm.nb_full[r]), 1);        // the row scanner
             tc::mbar_init(tc::smem_u32(&sm.nb_empty[r]), NGATH);   // every gather warp has read it
@@ -207,6 +256,10 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
             tc::mbar_init(tc::smem_u32(&sm.p_empty[b]), 1);
             tc::mbar_init(tc::smem_u32(&sm.o_step[b]), 1);
         }
+        tc::mbar_init(tc::smem_u32(&sm.resc_done), 4);
+        *reinterpret_cast<uint32_t*>(&sm.resc_flag[0][0]) = 0u;
+        *reinterpret_cast<uint32_t*>(&sm.resc_flag[1][0]) = 0u;
+        sm.resc_seq = 0;
         sm.abort = 0;
         tc::mbar_init_fence();
     }
@@ -363,10 +416,8 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
     } else if (warp == 10) {
         // ===================================================== PV issuer
         if (lane == 0) {
-            uint32_t g = 0, qn = 0;
-            // test hook: with a stall injected, wait first on a barrier that nothing completes, so the
-            // bounded wait runs out while the producers, S issuers and softmax warps are mid-stream
-            bool ok = g_sparse_mla_stall == 0 || tc::mbar_wait(tc::smem_u32(&sm.never), 0, abort_flag);
+            uint32_t g = 0, qn = 0, nreq = 0;
+            bool ok = true;
             for (int i = blockIdx.x; i < n_rows && ok && !*abort_flag; i += gridDim.x, ++qn) {
                 if (!tc::mbar_wait(tc::smem_u32(&sm.q_full), qn & 1, abort_flag)) { ok = false; break; }
                 const int nb = sm.nb;
@@ -377,6 +428,19 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
                         (b == 0 && !tc::mbar_wait(tc::smem_u32(&sm.o_free), (qn & 1) ^ 1, abort_flag))) {
                         ok = false;
                         break;
+                    }
+                    // a softmax warp raised a head's running max in this block: O^T is rescaled by the
+                    // softmax warps (after the previous PV) before this PV adds to it
+                    const uint32_t fl = *reinterpret_cast<volatile uint32_t*>(&sm.resc_flag[sb][0]);
+                    if (fl != 0u) {
+                        *reinterpret_cast<volatile uint32_t*>(&sm.resc_flag[sb][0]) = 0u;
+                        sm.resc_mask = fl;
+                        sm.resc_g = (int)g;
+                        st_release(&sm.resc_seq, (int)++nreq);
+                        if (!tc::mbar_wait(tc::smem_u32(&sm.resc_done), (nreq - 1) & 1, abort_flag)) {
+                            ok = false;
+                            break;
+                        }
                     }
                     tc::fence_proxy_async();
                     tc::fence_after();
@@ -416,8 +480,10 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
         // published up to two queries ahead of the producers; rows two queries
         // ahead are prefetched into L2.
         uint32_t qn = 0;
-        bool ok = true;
-        for (int i = blockIdx.x; i < n_rows; i += gridDim.x, ++qn) {
+        // test hook: with a stall injected, first wait on the end-of-kernel barrier, which completes
+        // only after the MMA issuers have left their loops, so the bounded waits of every role run out
+        bool ok = g_sparse_mla_stall == 0 || warp_wait(tc::smem_u32(&sm.drain), 0, abort_flag);
+        for (int i = blockIdx.x; i < n_rows && ok; i += gridDim.x, ++qn) {
             if (__shfl_sync(0xffffffffu, *abort_flag, 0)) break;
             const int r = qn & 1;
             if (!warp_wait(tc::smem_u32(&sm.nb_empty[r]), ((qn >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
@@ -465,14 +531,37 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
         // ===================================================== softmax / correction / epilogue
         regs_inc<168>();
         // Row h = 16*wid + (lane & 15) (head); lane half hs = lane >> 4 owns
-        // slots 32*hs .. 32*hs+31 of the block.  `bad` is sticky per thread and
-        // ORed across the four warps at every named barrier (bar.red.or).
+        // slots 32*hs .. 32*hs+31 of the block.  `bad` is sticky per warp; a warp
+        // that sees it leaves the block loop, and the four warps OR it at the
+        // named barriers (bar.red.or) of every query's start and end.
         const int wid = warp - 4;                   // TMEM subpartition
         const int hs = lane >> 4;
         const int h = wid * 16 + (lane & 15);       // head of this thread
         const uint32_t lane_base = (uint32_t)(wid * 32) << 16;
         uint32_t g = 0, qn = 0;
         bool bad = false;
+        int served = 0;                             // rescale requests this warp has served
+        // Bounded wait of a softmax warp that serves rescale requests meanwhile (the awaited phase
+        // can depend on the PV that a request holds back).
+        auto sm_wait = [&](uint32_t addr, uint32_t parity) -> bool {
+            const uint64_t t0 = tc::globaltimer_ns();
+            for (uint32_t it = 0;; ++it) {
+                uint32_t st = 0;
+                if (lane == 0) {
+                    st = tc::mbar_try(addr, parity) ? 1u : 0u;
+                    if (!st && ld_acquire(&sm.resc_seq) != served) st = 2u;
+                    if (!st && (it & 15u) == 15u && (*abort_flag || tc::globaltimer_ns() - t0 > tc::WAIT_LIMIT_NS))
+                        st = 3u;
+                }
+                st = __shfl_sync(0xffffffffu, st, 0);
+                if (st == 1u) return true;
+                if (st == 3u) return false;
+                if (st == 2u) {
+                    if (!serve_rescale(sm, tmem + lane_base, abort_flag)) return false;
+                    ++served;
+                }
+            }
+        };
         for (int i = blockIdx.x; i < n_rows; i += gridDim.x, ++qn) {
             bad = bad || !warp_wait(tc::smem_u32(&sm.q_full), qn & 1, abort_flag);
             if (wg_or(bad)) { bad = true; break; }
@@ -482,11 +571,14 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
             float m_ref = -INFINITY, l = 0.f;       // m_ref equal in both lanes of a row; l partial
             for (int b = 0; b < nb; ++b, ++g) {
                 const int s = g % NSTAGE, sb = g % NSB;
-                const int cb = g & 1;
                 float x[32];
-                bad = bad || !warp_wait(tc::smem_u32(&sm.s_full[sb]), (g / NSB) & 1, abort_flag);
-                if (!bad) {
-                    tc::fence_after();
+                // P^T buffer free (PV of block g-2 done), then S of this block; both waits serve
+                // rescale requests, as neither holds live values
+                bad = bad || !sm_wait(tc::smem_u32(&sm.p_empty[sb]), ((g / NSB) & 1) ^ 1) ||
+                      !sm_wait(tc::smem_u32(&sm.s_full[sb]), (g / NSB) & 1);
+                if (bad) break;
+                tc::fence_after();
+                {
                     // lane l < 16 holds the K-half-0 row, lane l+16 the K-half-1 row of the
                     // same head; swap halves so that each keeps 32 slots of the sum
                     uint32_t va[32], vb[32];
@@ -499,42 +591,37 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
                         const float recv = __uint_as_float(__shfl_xor_sync(0xffffffffu, send, 16));
                         x[j] = __uint_as_float(hs ? vb[j] : va[j]) + recv;
                     }
-                    tc::fence_before();
-                    __syncwarp();
-                    if (lane == 0) tc::mbar_arrive(tc::smem_u32(&sm.s_free[sb]));
-                    bad = !warp_wait(tc::smem_u32(&sm.kv_full[s]), (g / NSTAGE) & 1, abort_flag);
                 }
-                const uint32_t mask =
-                    bad ? 0u
-                        : (uint32_t)(*reinterpret_cast<volatile uint64_t*>(&sm.mask[s][0]) >> (32 * hs));
-                const float thr = m_ref + TAU;        // -inf for a row that has seen no valid slot yet
+                tc::fence_before();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(tc::smem_u32(&sm.s_free[sb]));
+                // the block's valid-slot mask (S of the block was computed, so its copies have landed)
+                bad = !warp_wait(tc::smem_u32(&sm.kv_full[s]), (g / NSTAGE) & 1, abort_flag);
+                if (bad) break;
+                const uint32_t mask = (uint32_t)(*reinterpret_cast<volatile uint64_t*>(&sm.mask[s][0]) >> (32 * hs));
                 // every slot of the warp's half-blocks valid (all but a row's last block): x stays
                 // unscaled, the exceed test runs on the block max (scaling by a positive factor
                 // and rounding keep the order) and the scale is fused into the exponent's FMA
                 const bool full = __all_sync(0xffffffffu, mask == 0xffffffffu) && scale_log2 > 0.f;
-                bool exceed = false;
-                if (full) {
-                    float bm = x[0];
+                if (!full) {
 #pragma unroll
-                    for (int j = 1; j < 32; ++j) bm = fmaxf(bm, x[j]);
-                    exceed = bm * scale_log2 > thr;
-                } else {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        x[j] = ((mask >> j) & 1u) ? x[j] * scale_log2 : -INFINITY;
-                        exceed |= x[j] > thr;
-                    }
+                    for (int j = 0; j < 32; ++j) x[j] = ((mask >> j) & 1u) ? x[j] * scale_log2 : -INFINITY;
                 }
-                // common case: no running max moves, one barrier per block
-                if (wg_or(bad || exceed)) {
-                    if (wg_or(bad)) { bad = true; break; }
-                    float bmax = -INFINITY;
+                float t16[16];
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) bmax = fmaxf(bmax, x[j]);
-                    if (full) bmax *= scale_log2;
-                    bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, 16));
-                    float alpha = 1.f;
-                    bool need = false;
+                for (int j = 0; j < 16; ++j) t16[j] = fmaxf(x[j], x[j + 16]);
+#pragma unroll
+                for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+                    for (int j = 0; j < w; ++j) t16[j] = fmaxf(t16[j], t16[j + w]);
+                const float lmax = full ? t16[0] * scale_log2 : t16[0];
+                // the running max of a head moves only when a slot beats it by more than 2^TAU
+                // (-inf until the row's first valid slot); the warp decides alone, and a move of a
+                // max that O^T already depends on is passed to the PV issuer as a rescale request
+                float alpha = 1.f;
+                bool need = false;
+                if (__any_sync(0xffffffffu, lmax > m_ref + TAU)) {
+                    const float bmax = fmaxf(lmax, __shfl_xor_sync(0xffffffffu, lmax, 16));
                     if (bmax > m_ref + TAU) {
                         if (m_ref != -INFINITY) {          // O^T holds this head's earlier slots
                             alpha = fast_exp2(m_ref - bmax);
@@ -543,32 +630,14 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
                         }
                         m_ref = bmax;
                     }
-                    if (hs == 0) sm.alpha[cb][h] = alpha;
-                    if (wg_or(need)) {
-                        // O^T must hold the previous block's PV before it is rescaled
-                        const uint32_t gp = g - 1;
-                        bad = !warp_wait(tc::smem_u32(&sm.o_step[gp % NSB]), (gp / NSB) & 1, abort_flag);
-                        if (!bad) {
-                            tc::fence_after();
-                            for (int t = 0; t < 4; ++t)
-                                for (int c0 = 0; c0 < HP; c0 += 32) {
-                                    uint32_t o[32];
-                                    const uint32_t ta = tmem + lane_base + TM_O + 64 * t + c0;
-                                    tc::tmem_ld32(ta, o);
-                                    tc::tmem_wait_ld();
-#pragma unroll
-                                    for (int j = 0; j < 32; ++j)
-                                        o[j] = __float_as_uint(__uint_as_float(o[j]) * sm.alpha[cb][c0 + j]);
-                                    tc::tmem_st32(ta, o);
-                                }
-                            tc::tmem_wait_st();
-                            tc::fence_before();
-                        }
-                    }
                 }
+                const bool warp_need = __any_sync(0xffffffffu, need);
                 // P^T row h, slots 32*hs .. 32*hs+31: 64 bytes, 16-byte units 4hs .. 4hs+3
-                bad = bad || !warp_wait(tc::smem_u32(&sm.p_empty[sb]), ((g / NSB) & 1) ^ 1, abort_flag);
-                if (!bad) {
+                if (warp_need) {
+                    if (hs == 0) sm.alpha[sb][h] = alpha;
+                    if (lane == 0) sm.resc_flag[sb][wid] = 1;
+                }
+                {
                     uint32_t pk[16];
                     float2 ps[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
                     const bool live = m_ref != -INFINITY;
@@ -603,7 +672,7 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
             }
             if (wg_or(bad)) { bad = true; break; }
             // ---- epilogue: O^T / l -> bf16 out, lse
-            bad = !warp_wait(tc::smem_u32(&sm.o_full), qn & 1, abort_flag);
+            bad = !sm_wait(tc::smem_u32(&sm.o_full), qn & 1);
             const float lt = l + __shfl_xor_sync(0xffffffffu, l, 16);
             if (hs == 0) {
                 sm.inv_l[h] = lt > 0.f ? 1.f / lt : 0.f;

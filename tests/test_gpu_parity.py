@@ -366,6 +366,52 @@ def test_sparse_mla_holes_and_late_rescales():
     assert len(big) > 10
 
 
+def test_sparse_mla_rescales_from_several_warps_and_last_blocks():
+    """Running-max moves that O^T already depends on, raised in one block by heads of different softmax
+    warps at once, again for a head in a later block, and in a row's last block (whose rescale must be
+    done before the last PV, while the softmax warps wait for the epilogue)."""
+    wl = workloads.custom("mla_rescales", 12, (700,), n_heads=64)
+    inp = workloads.indexer_inputs(wl)
+    ql = workloads.q_lat(wl)
+    kv = inp.kv_lat.float().clone()
+    T, W = wl.T, 640
+    rng = np.random.default_rng(5)
+    idx = np.full((T, W), -1, np.int32)
+    for i in range(T):
+        n = min(i + 1, W)
+        idx[i, :n] = np.sort(rng.choice(i + 1, n, replace=False)).astype(np.int32)
+    used = set()
+
+    def aim(i, h, j, logit):
+        r = int(idx[i, j])
+        if r < 0 or r in used:
+            return False
+        qh = ql[i, h].float()
+        kv[r] = qh / qh.norm() * logit / wl.scale / qh.norm()
+        used.add(r)
+        return True
+
+    hits = 0
+    for i in range(200, T, 3):
+        n = min(i + 1, W)
+        nb = (n + 63) // 64
+        b1 = 1 + i % max(1, nb - 2)
+        for k, h in enumerate((i % 64, (i + 21) % 64, (i + 42) % 64)):      # three warps, one block
+            hits += aim(i, h, b1 * 64 + 3 + 5 * k, 12.0 + 3.0 * k)
+        if b1 + 1 < nb - 1:                                                   # the same head again later
+            hits += aim(i, i % 64, (b1 + 1) * 64 + 9, 26.0)
+        hits += aim(i, (i + 7) % 64, n - 1, 20.0)                             # the row's last slot
+    kv_b = kv.to(torch.bfloat16)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    out, lse = K.sparse_mla_fwd(ql.cuda(), kv_b.cuda(), torch.from_numpy(idx).cuda(), wl.scale, status=st)
+    assert K.check_status(st) == 0
+    rows = np.arange(T)
+    out_o, lse_o = O.sparse_attention(ql.float().numpy(), kv_b.float().numpy(), idx, wl.scale, rows)
+    mx, mean, le = KP.attention_check(out.float().cpu().numpy(), lse.cpu().numpy(), out_o, lse_o)
+    assert mx <= KP.OUT_MAX_ABS and mean <= KP.OUT_MEAN_ABS and le <= KP.LSE_ABS, (mx, mean, le)
+    assert hits > 200
+
+
 @pytest.mark.parametrize("H, W", [(48, 130), (16, 256), (64, 2176)])
 def test_one_query_per_cta_launches(H, W):
     """Launches with at most one query per CTA (as a decode step makes) take the kernel's one-query instance,

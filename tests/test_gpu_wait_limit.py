@@ -61,7 +61,7 @@ def test_stalled_waits_time_out_and_the_next_calls_match_a_clean_run():
     assert st == 0
     assert torch.equal(idx1, idx0)
 
-    # sparse attention: its PV issuer never starts, the ring and both S buffers fill up behind it
+    # sparse attention: its row scanner never publishes a block count, so every role's wait runs out
     K.debug_inject_stall(K.STALL_SPARSE_MLA)
     try:
         status.zero_()
