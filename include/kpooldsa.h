@@ -375,7 +375,7 @@ int kpool_measure_l2_reduce(float* buf, int32_t rows, const int32_t* row_ids, in
  * TMEM is freed, so the context stays usable.  This hook makes that path run
  * on demand: with KPOOL_STALL_SCORE set, every later launch of the tcgen05
  * scoring kernel (dsa_index with d_idx = 128) first waits on a barrier that
- * nothing completes, in its MMA issuer; with KPOOL_STALL_SPARSE_MLA, every
+ * nothing completes, in its TMA producer; with KPOOL_STALL_SPARSE_MLA, every
  * later sparse_mla_fwd / sparse_mla_fwd_rows launch does the same in its row
  * scanner (the barrier completes only after the kernel has aborted).  Such a launch takes about two seconds, ends with
  * KPOOL_ERR_TIMEOUT and leaves its outputs undefined.  mask = 0 restores

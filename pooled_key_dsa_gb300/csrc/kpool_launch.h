@@ -61,7 +61,7 @@ int launch_sparse_mla_bwd(const uint16_t* q_lat, const uint16_t* kv_lat, const i
                           cudaStream_t stream);
 
 // Test hooks of the bounded waits: nonzero makes the next launches of the kernel wait first on a barrier
-// that cannot complete in time (tcgen05 scoring: its MMA issuer; sparse MLA: its row scanner).
+// that cannot complete in time (tcgen05 scoring: its TMA producer; sparse MLA: its row scanner).
 int set_score_tc_stall(int on);
 int set_sparse_mla_stall(int on);
 

@@ -140,7 +140,7 @@ __device__ __forceinline__ void score_chunk(const uint32_t (&v)[32], const float
     }
 }
 
-// Nonzero: the next launches stall their MMA issuer on a barrier that is never
+// Nonzero: the next launches stall their TMA producer on a barrier that is never
 // completed (test of the bounded waits; set with set_score_tc_stall).
 __device__ int g_score_tc_stall = 0;
 

@@ -50,7 +50,7 @@ def test_stalled_waits_time_out_and_the_next_calls_match_a_clean_run():
     out0, lse0 = K.sparse_mla_fwd(q, dev["kv_lat"], idx0, wl.scale, status=status)
     assert K.check_status(status) == 0
 
-    # scoring: its MMA issuer never sees its first operands arrive
+    # scoring: its TMA producer never loads, so the MMA issuer and the epilogue warps time out too
     K.debug_inject_stall(K.STALL_SCORE)
     try:
         _, st = _index(wl, dev, p, layout, kp)
