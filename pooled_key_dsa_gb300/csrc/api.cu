@@ -3,10 +3,22 @@
 #include <cstdint>
 #include <cstring>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "kpool_common.cuh"
 #include "kpool_launch.h"
 
 namespace kpool {
+
+// NVTX range around the host side of one call (the enqueue of its launches), named after the
+// call, so that a timeline tool can group each call's kernels under it.  Without a tool attached
+// a push/pop costs a few nanoseconds.
+struct Range {
+    explicit Range(const char* name) { nvtxRangePushA(name); }
+    ~Range() { nvtxRangePop(); }
+    Range(const Range&) = delete;
+    Range& operator=(const Range&) = delete;
+};
 
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
@@ -74,6 +86,7 @@ int kpool_workspace_offsets(const kpool_params* p, int32_t T, int32_t n_docs, kp
 
 int kpool_build(const void* k, const float* gate, const float* ape, const int32_t* cu_seqlens, int32_t n_docs,
                 int32_t T, const kpool_params* p, float* kpool_out, kpool_layout* layout, kpool_stream_t stream) {
+    const Range range("kpool_build");
     if (!params_ok(p)) return KPOOL_ERR_INVALID_ARG;
     if (!layout_ok(layout) || layout->n_docs != n_docs || layout->T != T || layout->cu_seqlens != cu_seqlens)
         return KPOOL_ERR_INVALID_ARG;
@@ -86,6 +99,7 @@ int kpool_build(const void* k, const float* gate, const float* ape, const int32_
 int dsa_index(const void* q_idx, const float* w, const float* kpool, const kpool_layout* layout, int32_t topk,
               const kpool_params* p, void* workspace, size_t workspace_bytes, int32_t* indices, int32_t W,
               kpool_stream_t stream) {
+    const Range range("dsa_index");
     if (!params_ok(p) || !layout_ok(layout)) return KPOOL_ERR_INVALID_ARG;
     const int tk = topk > 0 ? topk : p->topk;
     const int T = layout->T;
@@ -128,6 +142,7 @@ int dsa_index(const void* q_idx, const float* w, const float* kpool, const kpool
 int sparse_mla_fwd_rows(const void* q_lat, const void* kv_lat, const int32_t* indices, int32_t W, int32_t n_rows,
                         int32_t T, int32_t n_heads, float scale, void* out, float* lse, int32_t* status,
                         kpool_stream_t stream) {
+    const Range range("sparse_mla_fwd");
     if (n_rows < 0 || T < 0 || W < 1 || n_heads < 1 || n_heads > 64) return KPOOL_ERR_SHAPE;
     if (n_rows > 0 && (!q_lat || !kv_lat || !indices || !out || !lse)) return KPOOL_ERR_INVALID_ARG;
     if (!aligned(q_lat, 16) || !aligned(kv_lat, 16) || !aligned(out, 16) || !aligned(indices, 4))
@@ -146,6 +161,7 @@ int sparse_mla_fwd(const void* q_lat, const void* kv_lat, const int32_t* indices
 int sparse_mla_bwd(const void* q_lat, const void* kv_lat, const int32_t* indices, int32_t W, int32_t T,
                    int32_t n_heads, float scale, const void* out, const float* lse, const void* dout, void* dq,
                    float* dkv, float* delta, int32_t* status, kpool_stream_t stream) {
+    const Range range("sparse_mla_bwd");
     if (T < 0 || W < 1 || n_heads < 1 || n_heads > 64) return KPOOL_ERR_SHAPE;
     if (T > 0 && (!q_lat || !kv_lat || !indices || !out || !lse || !dout || !dq || !dkv || !delta))
         return KPOOL_ERR_INVALID_ARG;
@@ -210,6 +226,7 @@ int kpool_paged_append(const void* k, const float* gate, const float* ape, const
                        const int32_t* pool_seq, const int32_t* pool_idx, int32_t n_items, const int32_t* block_table,
                        int32_t max_pages, int32_t n_pages, const kpool_params* p, uint8_t* k8_cache, float* sk_cache,
                        int32_t* status, kpool_stream_t stream) {
+    const Range range("kpool_paged_append");
     if (!decode_shape_ok(p)) return p ? KPOOL_ERR_SHAPE : KPOOL_ERR_INVALID_ARG;
     if (n_items < 0 || max_pages < 1 || n_pages < 1) return KPOOL_ERR_SHAPE;
     if (n_items == 0) return KPOOL_OK;
@@ -225,6 +242,7 @@ int dsa_decode_index(const void* q_idx, const float* w, const uint8_t* k8_cache,
                      int32_t n_pages, const int32_t* block_table, int32_t max_pages, const int32_t* seq_lens,
                      int32_t B, int32_t topk, const kpool_params* p, void* workspace, size_t workspace_bytes,
                      int32_t* indices, int32_t W, int32_t* status, kpool_stream_t stream) {
+    const Range range("dsa_decode_index");
     if (!p) return KPOOL_ERR_INVALID_ARG;
     if (!decode_shape_ok(p)) return KPOOL_ERR_SHAPE;
     if (B < 0 || max_pages < 1 || n_pages < 1 || topk < 1 || W < KPOOL * topk + KPOOL - 1 || (W & 3) != 0)
@@ -253,6 +271,7 @@ int dsa_decode_index(const void* q_idx, const float* w, const uint8_t* k8_cache,
 
 int mla_absorb_q(const void* q_nope, const void* w_kv_b, int32_t T, int32_t n_heads, int32_t d_nope, int32_t d_v,
                  void* q_lat, int32_t* status, kpool_stream_t stream) {
+    const Range range("mla_absorb_q");
     if (T < 0 || !mla_proj_shape_ok(n_heads, d_nope, d_v)) return KPOOL_ERR_SHAPE;
     if (T > 0 && (!q_nope || !w_kv_b || !q_lat)) return KPOOL_ERR_INVALID_ARG;
     if (!aligned(q_nope, 16) || !aligned(w_kv_b, 16) || !aligned(q_lat, 16)) return KPOOL_ERR_ALIGN;
@@ -262,6 +281,7 @@ int mla_absorb_q(const void* q_nope, const void* w_kv_b, int32_t T, int32_t n_he
 
 int mla_v_proj(const void* o_lat, const void* w_kv_b, int32_t T, int32_t n_heads, int32_t d_nope, int32_t d_v,
                void* o_v, int32_t* status, kpool_stream_t stream) {
+    const Range range("mla_v_proj");
     if (T < 0 || !mla_proj_shape_ok(n_heads, d_nope, d_v)) return KPOOL_ERR_SHAPE;
     if (T > 0 && (!o_lat || !w_kv_b || !o_v)) return KPOOL_ERR_INVALID_ARG;
     if (!aligned(o_lat, 16) || !aligned(w_kv_b, 16) || !aligned(o_v, 16)) return KPOOL_ERR_ALIGN;
@@ -272,6 +292,7 @@ int mla_v_proj(const void* o_lat, const void* w_kv_b, int32_t T, int32_t n_heads
 int kpool_forward_host(const kpool_host_io* h, const kpool_dev_io* d, int32_t n_docs, int32_t T,
                        const kpool_params* p, int32_t n_chunks, kpool_stream_t s_in, kpool_stream_t s_compute,
                        kpool_stream_t s_out) {
+    const Range range("kpool_forward_host");
     if (!h || !d || !p || !d->layout) return KPOOL_ERR_INVALID_ARG;
     if (T < 1 || n_docs < 1 || n_chunks < 1 || n_chunks > KPOOL_MAX_CHUNKS) return KPOOL_ERR_SHAPE;
     if (!h->k || !h->gate || !h->ape || !h->cu_seqlens || !h->q_idx || !h->w || !h->q_lat || !h->kv_lat ||
