@@ -55,7 +55,10 @@
 //              shared memory in the operand layout; the epilogue writes O^T / l
 //              as bf16 straight from TMEM, both 32-column halves of a tile
 //              loaded under one wait (lane pairs swap values so that every
-//              store covers two 64-byte runs of output rows).
+//              store covers two 64-byte runs of output rows), and releases
+//              O^T to the next query's PV once its last tile is in registers.
+//              1/l is kept per query parity, so a query needs two named
+//              barriers (its start and the end of its blocks).
 //   warps 8-9  S issuers (warp 8 also owns the TMEM allocation)
 //   warp 10    PV issuer
 //   warp 11    row scanner: block count and range check of each query's
@@ -110,7 +113,7 @@ struct Small {
     uint32_t resc_mask;                         // flags of the outstanding request
     int resc_g;                                 // block of the outstanding request
     int resc_seq;                               // requests issued so far
-    alignas(16) float inv_l[HP];
+    alignas(16) float inv_l[2][HP];             // per query parity: 1/l of every head
 };
 constexpr int SMEM_BYTES = OFF_SMALL + (int)sizeof(Small) + 1024;   // + alignment slack
 static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
@@ -237,7 +240,7 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
 
     if (tid == 0) {
         tc::mbar_init(tc::smem_u32(&sm.q_full), NGATH);   // each producer warp: its Q columns stored (+ nb)
-        tc::mbar_init(tc::smem_u32(&sm.q_empty), 4);      // two S issuers, PV issuer, softmax
+        tc::mbar_init(tc::smem_u32(&sm.q_empty), 7);      // two S issuers, PV issuer, four softmax warps
         tc::mbar_init(tc::smem_u32(&sm.o_full), 1);
         tc::mbar_init(tc::smem_u32(&sm.o_free), 4);
         tc::mbar_init(tc::smem_u32(&sm.drain), 3);
@@ -566,8 +569,8 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
             bad = bad || !warp_wait(tc::smem_u32(&sm.q_full), qn & 1, abort_flag);
             if (wg_or(bad)) { bad = true; break; }
             const int nb = sm.nb;
-            wg_or(false);                           // every warp has read nb
-            if (tid == 128) tc::mbar_arrive(tc::smem_u32(&sm.q_empty));
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(tc::smem_u32(&sm.q_empty));   // this warp has read nb
             float m_ref = -INFINITY, l = 0.f;       // m_ref equal in both lanes of a row; l partial
             for (int b = 0; b < nb; ++b, ++g) {
                 const int s = g % NSTAGE, sb = g % NSB;
@@ -675,7 +678,7 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
             bad = !sm_wait(tc::smem_u32(&sm.o_full), qn & 1);
             const float lt = l + __shfl_xor_sync(0xffffffffu, l, 16);
             if (hs == 0) {
-                sm.inv_l[h] = lt > 0.f ? 1.f / lt : 0.f;
+                sm.inv_l[qn & 1][h] = lt > 0.f ? 1.f / lt : 0.f;
                 if (h < H)
                     lse[(int64_t)i * H + h] = lt > 0.f ? (m_ref + log2f(lt)) * 0.69314718055994530942f : -INFINITY;
             }
@@ -701,12 +704,17 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
 #pragma unroll
                     for (int j = 0; j < 32; ++j) o[0][j] = o[1][j] = 0u;
                 }
+                if (t == 3) {                        // O^T is read: the next query's PV may start
+                    tc::fence_before();
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(tc::smem_u32(&sm.o_free));
+                }
 #pragma unroll
                 for (int hf = 0; hf < 2; ++hf) {
                     const int c0 = 32 * hf;
 #pragma unroll
                     for (int j = 0; j < 32; j += 2) {
-                        const float2 il = *reinterpret_cast<const float2*>(&sm.inv_l[c0 + j]);
+                        const float2 il = *reinterpret_cast<const float2*>(&sm.inv_l[qn & 1][c0 + j]);
                         const float a = __uint_as_float(o[hf][j]) * il.x;
                         const float b = __uint_as_float(o[hf][j + 1]) * il.y;
                         const float recv = __shfl_xor_sync(0xffffffffu, odd ? a : b, 1);
@@ -716,10 +724,6 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
                     }
                 }
             }
-            tc::fence_before();
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(tc::smem_u32(&sm.o_free));
-            wg_or(false);                           // inv_l is rewritten next query
         }
         if (bad) fail(sm, status);
     }
