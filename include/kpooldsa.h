@@ -60,7 +60,9 @@ typedef enum {
     KPOOL_ERR_INDEX_RANGE = 5,  /* index row entry outside [-1, T)           */
     KPOOL_ERR_TIMEOUT = 6,      /* a bounded device wait expired             */
     KPOOL_ERR_CUDA = 7,         /* a CUDA runtime call failed                */
-    KPOOL_ERR_WORKSPACE = 8     /* workspace null or too small               */
+    KPOOL_ERR_WORKSPACE = 8,    /* workspace null or too small               */
+    KPOOL_ERR_CHECK = 9         /* internal bounds check failed (library
+                                   built with KPOOL_CHECKED only)             */
 } kpool_status;
 
 /* Layer parameters.  kpool must be 4 (index_kpool); d_idx is 64 or 128;

@@ -3,6 +3,12 @@
 Each ``csrc/*.cu`` file is compiled by nvcc in parallel (skipped when its
 object is newer than every source and header), then linked into one shared
 library with the C ABI of ``include/kpooldsa.h``.
+
+``build(checked=True)`` builds the same sources with ``-DKPOOL_CHECKED`` into
+``_lib/libkpooldsa_checked.so``: internal bounds checks on the indexer's
+computed indices then record ``KPOOL_ERR_CHECK`` in the status word instead of
+being compiled out (a stand-in for a memory checker, which this pool does not
+offer).
 """
 from __future__ import annotations
 
@@ -19,6 +25,8 @@ INCLUDE = os.path.join(ROOT, "include")
 LIBDIR = os.path.join(PKG, "_lib")
 OBJDIR = os.path.join(LIBDIR, "obj")
 LIB = os.path.join(LIBDIR, "libkpooldsa.so")
+OBJDIR_CHECKED = os.path.join(LIBDIR, "obj_checked")
+LIB_CHECKED = os.path.join(LIBDIR, "libkpooldsa_checked.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2", "--expt-relaxed-constexpr",
@@ -37,15 +45,18 @@ def _deps_mtime() -> float:
     return max(os.path.getmtime(f) for f in files)
 
 
-def build(verbose: bool = False, force: bool = False, extra_flags=()) -> str:
+def build(verbose: bool = False, force: bool = False, extra_flags=(), checked: bool = False) -> str:
     """Compile and link; returns the library path.  Raises on a compiler error."""
-    os.makedirs(OBJDIR, exist_ok=True)
+    objdir, lib = (OBJDIR_CHECKED, LIB_CHECKED) if checked else (OBJDIR, LIB)
+    if checked:
+        extra_flags = (*extra_flags, "-DKPOOL_CHECKED")
+    os.makedirs(objdir, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     newest = _deps_mtime()
     cc = nvcc()
 
     def compile_one(src):
-        obj = os.path.join(OBJDIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(objdir, os.path.basename(src)[:-3] + ".o")
         if not force and os.path.exists(obj) and os.path.getmtime(obj) >= newest:
             return obj
         cmd = [cc, *NVCC_FLAGS, *extra_flags, "-c", src, "-o", obj]
@@ -58,12 +69,12 @@ def build(verbose: bool = False, force: bool = False, extra_flags=()) -> str:
 
     with ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
         objs = list(ex.map(compile_one, srcs))
-    if force or not os.path.exists(LIB) or os.path.getmtime(LIB) < max(os.path.getmtime(o) for o in objs):
-        cmd = [cc, *ARCH, "-shared", "-o", LIB, *objs, "-ldl"]
+    if force or not os.path.exists(lib) or os.path.getmtime(lib) < max(os.path.getmtime(o) for o in objs):
+        cmd = [cc, *ARCH, "-shared", "-o", lib, *objs, "-ldl"]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
             raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    return LIB
+    return lib
 
 
 if __name__ == "__main__":

@@ -413,12 +413,13 @@ const char* kpool_strerror(int code) {
         case KPOOL_ERR_TIMEOUT: return "device wait timed out";
         case KPOOL_ERR_CUDA: return "CUDA error";
         case KPOOL_ERR_WORKSPACE: return "workspace missing or too small";
+        case KPOOL_ERR_CHECK: return "internal bounds check failed";
         default: return "unknown error";
     }
 }
 
 // The tags after the arch name identify the kernel generations (used to match
 // stored profiler counters to the code that produced them).
-const char* kpool_version(void) { return "kpooldsa 0.15 sm_103a mla-tc11 score-tc3 select4 proj1 bwd4 decode2 pool2 hadamard3"; }
+const char* kpool_version(void) { return "kpooldsa 0.16 sm_103a mla-tc11 score-tc3 select5 proj1 bwd4 decode2 pool2 hadamard3"; }
 
 }  // extern "C"

@@ -19,6 +19,19 @@ __device__ __forceinline__ void set_status(int32_t* status, int code) {
     if (status != nullptr) atomicCAS(reinterpret_cast<int*>(status), 0, code);
 }
 
+// Internal bounds checks.  In the KPOOL_CHECKED build a failed check records
+// KPOOL_ERR_CHECK in the call's status word and the caller skips the access;
+// in the default build the check is compiled out (every checked index holds by
+// construction there, and the checked build's tests show it).
+#ifdef KPOOL_CHECKED
+__device__ __forceinline__ bool in_bounds(bool ok, int32_t* status) {
+    if (!ok) set_status(status, KPOOL_ERR_CHECK);
+    return ok;
+}
+#else
+__device__ __forceinline__ bool in_bounds(bool, int32_t*) { return true; }
+#endif
+
 // Number of (query, candidate pool) score slots before in-document position r:
 // sum over r' < r of floor((r'+1)/4) = sum_{m=1..r} floor(m/4).
 // With r = 4a + b: 4 * (0 + 1 + ... + (a-1)) + a * (b + 1).

@@ -97,7 +97,7 @@ __global__ void layout_fill_kernel(const int32_t* __restrict__ cu_seqlens, const
 __global__ void kpool_pool_kernel(const uint16_t* __restrict__ k, const float* __restrict__ gate,
                                   const float* __restrict__ ape, const int32_t* __restrict__ cu_pools,
                                   const int32_t* __restrict__ pool_tok_start, int n_docs, int max_pools,
-                                  int d_idx, float* __restrict__ kpool_out) {
+                                  int d_idx, float* __restrict__ kpool_out, int T, int32_t* status) {
     const int groups = d_idx >> 2;
     const int64_t gid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
     if (gid >= (int64_t)max_pools * groups) return;
@@ -110,6 +110,7 @@ __global__ void kpool_pool_kernel(const uint16_t* __restrict__ k, const float* _
         return;
     }
     const int t0 = pool_tok_start[p];
+    if (!in_bounds(t0 >= 0 && t0 + KPOOL <= T, status)) return;
     double lg[KPOOL][4], kv[KPOOL][4];
 #pragma unroll
     for (int j = 0; j < KPOOL; ++j) {
@@ -175,7 +176,7 @@ int launch_kpool_build(const void* k, const float* gate, const float* ape, const
     if (work > 0)
         kpool_pool_kernel<<<(unsigned)((work + 255) / 256), 256, 0, stream>>>(
             static_cast<const uint16_t*>(k), gate, ape, L.cu_pools, L.pool_tok_start, L.n_docs, L.max_pools,
-            d_idx, kpool_out);
+            d_idx, kpool_out, L.T, L.status);
     return cudaGetLastError() == cudaSuccess ? KPOOL_OK : KPOOL_ERR_CUDA;
 }
 

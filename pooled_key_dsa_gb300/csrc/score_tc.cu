@@ -156,7 +156,8 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_tc_kernel(
     const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k, const float* __restrict__ ws,
     const float* __restrict__ s_k, const int32_t* __restrict__ cu_seqlens, const int32_t* __restrict__ cu_pools,
     int n_docs, int max_pools, int T, const int64_t* __restrict__ pair_base, const int32_t* __restrict__ sched,
-    int topk, uint32_t b_box_bytes, uint32_t a_box_bytes, float* __restrict__ scores, int32_t* status) {
+    int topk, uint32_t b_box_bytes, uint32_t a_box_bytes, float* __restrict__ scores, int64_t n_scores,
+    int32_t* status) {
     constexpr int QG = 256 / HI;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -320,12 +321,14 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_tc_kernel(
                 float res[QG];
                 auto store = [&](int q) {
                     if constexpr (QG <= 8) {
-                        if (pool_local < qlim[q]) scores[qbase[q] + pool_local] = res[q] * sk;
+                        if (pool_local < qlim[q] && in_bounds(qbase[q] + pool_local < n_scores, status))
+                            scores[qbase[q] + pool_local] = res[q] * sk;
                     } else {
                         const int r = it.r0 + q;
                         const int n_i = (r + 1) / KPOOL;
-                        if (r < it.L && n_i > topk && pool_local < n_i)
-                            scores[row_base + pairs_before(r) + pool_local] = res[q] * sk;
+                        const int64_t o = row_base + pairs_before(r) + pool_local;
+                        if (r < it.L && n_i > topk && pool_local < n_i && in_bounds(o < n_scores, status))
+                            scores[o] = res[q] * sk;
                     }
                 };
                 if constexpr (QG <= 32) {
@@ -422,7 +425,7 @@ static int launch_tc(const uint8_t* q8, const float* ws, const uint8_t* k8, cons
     if (!make_map(&mq, q8, q_rows, b_rows) || !make_map(&mk, k8, k_rows, a_rows)) return KPOOL_ERR_CUDA;
     score_tc_kernel<HI><<<n_sm[dev], SC_THREADS, SC_SMEM, stream>>>(
         mq, mk, ws, s_k, L.cu_seqlens, L.cu_pools, L.n_docs, L.max_pools, L.T, pair_base, sched, topk, b_rows * 128,
-        a_rows * 128, scores, L.status);
+        a_rows * 128, scores, pairs_before(L.T), L.status);
     return cudaGetLastError() == cudaSuccess ? KPOOL_OK : KPOOL_ERR_CUDA;
 }
 

@@ -102,15 +102,28 @@ __device__ void pick_digit(SelectSmem& s, int nbins, uint32_t remaining) {
 // Where the positions of a row go: `pool(p)` is the first slot of pool p (the
 // pool's 4 positions are consecutive slots), `tok(pos)` the slot of position
 // pos of the document or sequence.
+// `put(row, rank, p)` writes the 4 slots of pool p as the rank-th kept pool; the checked build
+// also verifies that they fall inside the row and the slot range.
 struct DocMap {            // packed prefill: slots are global token rows
     int s_d;
+    int W, T;
+    int32_t* status;
     __device__ __forceinline__ int pool(int p) const { return s_d + KPOOL * p; }
     __device__ __forceinline__ int tok(int pos) const { return s_d + pos; }
+    __device__ __forceinline__ void put(int32_t* row, int rank, int p) const {
+        const int pos = pool(p);
+        if (in_bounds(KPOOL * rank + KPOOL <= W && pos >= 0 && pos + KPOOL <= T, status))
+            *reinterpret_cast<int4*>(row + KPOOL * rank) = make_int4(pos, pos + 1, pos + 2, pos + 3);
+    }
 };
 struct PageMap {           // paged decode: 128-token pages listed in the sequence's block table
     const int32_t* bt;
     __device__ __forceinline__ int pool(int p) const { return bt[p >> 5] * 128 + ((KPOOL * p) & 127); }
     __device__ __forceinline__ int tok(int pos) const { return bt[pos >> 7] * 128 + (pos & 127); }
+    __device__ __forceinline__ void put(int32_t* row, int rank, int p) const {
+        const int pos = pool(p);
+        *reinterpret_cast<int4*>(row + KPOOL * rank) = make_int4(pos, pos + 1, pos + 2, pos + 3);
+    }
 };
 
 constexpr int FAST_KPT = 32;                          // keys per thread on the register path
@@ -226,9 +239,88 @@ __device__ void select_registers(SelectSmem& s, const float* __restrict__ sc, in
         const uint32_t b = __ballot_sync(0xffffffffu, (take >> j) & 1u);
         const uint32_t rank = tab[8 * j + wid] + __popc(b & below);
         if (((take >> j) & 1u) && rank < (uint32_t)topk) {
-            const int pos = map.pool(SEL_THREADS * j + t);
-            *reinterpret_cast<int4*>(row + KPOOL * rank) = make_int4(pos, pos + 1, pos + 2, pos + 3);
+            map.put(row, (int)rank, SEL_THREADS * j + t);
         }
+    }
+}
+
+// Rows of up to 8192 candidates (with the row's offset in its first 16-byte unit) on the
+// contiguous path: thread t holds the UPT consecutive 16-byte units t*UPT .. t*UPT+UPT-1 of the
+// row, i.e. pools 4*UPT*t - off .. 4*UPT*t - off + 4*UPT - 1 in order (the row was copied into
+// shared memory with unit u at position (u % UPT) * 256 + u / UPT, so that these loads are
+// conflict-free).  The radix levels are those of the register path; the compaction is one
+// block scan of each thread's count of kept pools (and, for ties at K, of its count of ties),
+// after which a thread writes its kept pools in order, so the row still comes out ascending.
+template <int UPT, typename Map>
+__device__ void select_contig(SelectSmem& s, const float* __restrict__ buf, int n, int off, int topk,
+                              const Map& map, int32_t* __restrict__ row) {
+    constexpr int NC = 4 * UPT;
+    const int t = threadIdx.x;
+    const int p0 = NC * t - off;                     // pool of this thread's first key
+    uint32_t key[NC];
+#pragma unroll
+    for (int m = 0; m < UPT; ++m) {
+        const float4 v = reinterpret_cast<const float4*>(buf)[m * SEL_THREADS + t];
+        const float f[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const int p = p0 + 4 * m + e;
+            // positions outside the row (the first unit's leading floats, the slots past it) get
+            // key 0, which changes nothing, as on the register path
+            key[4 * m + e] = (p >= 0 && p < n) ? score_key(f[e]) : 0u;
+        }
+    }
+    fast_level(s, key, 0u, 0u, 21, 2048, (uint32_t)topk);
+    uint32_t prefix = s.digit << 21;
+    uint32_t rem = s.remaining, cnt = s.hist[s.digit & 2047u];
+    __syncthreads();
+    bool whole = cnt == rem;
+    if (!whole) {
+        fast_level(s, key, 0xFFE00000u, prefix, 10, 2048, rem);
+        prefix |= s.digit << 10;
+        rem = s.remaining;
+        cnt = s.hist[s.digit & 2047u];
+        __syncthreads();
+        whole = cnt == rem;
+    }
+    uint32_t K = prefix, need_eq = 0, n_eq = 0;
+    if (!whole) {
+        fast_level(s, key, 0xFFFFFC00u, prefix, 0, 1024, rem);
+        K = prefix | s.digit;
+        need_eq = s.remaining;
+        n_eq = s.hist[s.digit & 1023u];
+        __syncthreads();
+    }
+    // Positions outside the row hold key 0: never above K (K > 0 whenever a bin is kept whole), and
+    // left out of the ties, which leaves enough valid ties (with n > topk valid pools, fewer than
+    // topk keys exceed K = 0) and keeps the leading ones (pool < 0) from being taken first.
+    uint32_t gt = 0, eq = 0;
+#pragma unroll
+    for (int j = 0; j < NC; ++j) {
+        gt |= ((whole ? key[j] >= K : key[j] > K) ? 1u : 0u) << j;
+        eq |= (!whole && key[j] == K ? 1u : 0u) << j;
+    }
+    {
+        const int lo = p0 < 0 ? -p0 : 0, hi = n - p0 < NC ? n - p0 : NC;   // keys lo .. hi-1 are in the row
+        const uint32_t below_hi = hi >= 32 ? 0xFFFFFFFFu : (hi <= 0 ? 0u : (1u << hi) - 1u);
+        eq &= below_hi & ~((1u << lo) - 1u);
+    }
+    uint32_t take = gt;
+    if (n_eq != need_eq) {                           // ties at K: the lowest pool indices among them win
+        int tot;
+        const int before = block_excl_scan(__popc(eq), s.warp_tot, tot);
+        uint32_t e = eq;
+        for (int k = before; e != 0u && k < (int)need_eq; ++k) {
+            take |= e & (0u - e);                    // this thread's next tie, in pool order
+            e &= e - 1u;
+        }
+    } else {
+        take |= eq;
+    }
+    int tot;
+    int rank = block_excl_scan(__popc(take), s.warp_tot, tot);
+    for (uint32_t b = take; b != 0u && rank < topk; b &= b - 1u, ++rank) {
+        map.put(row, rank, p0 + __ffs(b) - 1);
     }
 }
 
@@ -367,8 +459,7 @@ __device__ __forceinline__ void select_chunked(SelectSmem& s, uint32_t* cand, in
             const uint32_t b = __ballot_sync(0xffffffffu, (take >> j) & 1u);
             const int rank = sel_base + (int)(tab[8 * j + wid] + __popc(b & below));
             if (((take >> j) & 1u) && rank < topk) {
-                const int pos = map.pool(c0 + SEL_THREADS * j + t);
-                *reinterpret_cast<int4*>(row + KPOOL * rank) = make_int4(pos, pos + 1, pos + 2, pos + 3);
+                map.put(row, rank, c0 + SEL_THREADS * j + t);
             }
         }
         __syncthreads();                             // tab is reused by the next chunk
@@ -422,6 +513,37 @@ __device__ __forceinline__ void prefetch_row(float* buf, const float* __restrict
     }
 }
 
+// Units per thread of the contiguous path for a row of n scores starting at float offset
+// start % 4 of its first unit (2, 3, 4, 6 or 8), or 0 when the row takes the register path.
+__device__ __forceinline__ int contig_upt(int64_t start, int n) {
+    const int f = n + (int)(start & 3);              // floats copied
+    if (f <= 2048) return 2;
+    if (f <= 3072) return 3;
+    if (f <= 4096) return 4;
+    if (f <= 6144) return 6;
+    if (f <= 8192) return 8;
+    return 0;
+}
+
+// As prefetch_row, with unit u of the row at position (u % upt) * 256 + u / upt of the buffer.
+__device__ __forceinline__ void prefetch_row_contig(float* buf, const float* __restrict__ scores, int64_t start,
+                                                    int n, int upt) {
+    const int64_t b0 = start * 4, b1 = (start + n) * 4;
+    const int64_t u0 = b0 >> 4, u1 = (b1 + 15) >> 4;
+    const char* base = reinterpret_cast<const char*>(scores);
+    const uint32_t dst0 = static_cast<uint32_t>(__cvta_generic_to_shared(buf));
+    for (int64_t u = u0 + threadIdx.x; u < u1; u += SEL_THREADS) {
+        const int64_t off = u * 16;
+        const int64_t rem = b1 - off;
+        const uint32_t bytes = rem < 16 ? (uint32_t)rem : 16u;
+        const int ur = (int)(u - u0);
+        const uint32_t posn = (uint32_t)((ur % upt) * SEL_THREADS + ur / upt);
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst0 + posn * 16u), "l"(base + off),
+                     "r"(bytes)
+                     : "memory");
+    }
+}
+
 __device__ __forceinline__ bool fast_row(const RowInfo& ri, int topk) {
     return ri.d >= 0 && ri.n > topk && ri.n <= FAST_MAX;
 }
@@ -445,27 +567,44 @@ __global__ void __launch_bounds__(SEL_THREADS, SEL_CTAS_PER_SM) select_kernel(co
                                                              const int32_t* __restrict__ cu_seqlens,
                                                              const int32_t* __restrict__ cu_pools,
                                                              const int32_t* __restrict__ tok_doc, int n_docs, int T,
-                                                             int topk, int32_t* __restrict__ indices, int W) {
+                                                             int topk, int32_t* __restrict__ indices, int W,
+                                                             int64_t n_scores, int32_t* status) {
     __shared__ SelectSmem s;
     extern __shared__ __align__(16) float rowbuf[];   // 2 x ROWBUF
     const int t = threadIdx.x;
     int i = blockIdx.x;
     if (i >= T) return;
+    // checked build: a row whose scores would fall outside the score triangle is left empty
+    auto scores_ok = [&](RowInfo& ri) {
+        if (ri.d >= 0 && ri.n > topk && !in_bounds(ri.start >= 0 && ri.start + ri.n <= n_scores, status)) ri.d = -1;
+    };
     RowInfo cur = row_info(i, pair_base, cu_seqlens, cu_pools, tok_doc, n_docs);
-    if (fast_row(cur, topk)) prefetch_row(rowbuf, scores, cur.start, cur.n);
+    scores_ok(cur);
+    if (fast_row(cur, topk)) {
+        const int upt = contig_upt(cur.start, cur.n);
+        if (upt) prefetch_row_contig(rowbuf, scores, cur.start, cur.n, upt);
+        else prefetch_row(rowbuf, scores, cur.start, cur.n);
+    }
     asm volatile("cp.async.commit_group;\n" ::: "memory");
     for (int k = 0; i < T; ++k, i += gridDim.x) {
         const int i2 = i + (int)gridDim.x;
         RowInfo nxt;
         nxt.d = -1;
-        if (i2 < T) nxt = row_info(i2, pair_base, cu_seqlens, cu_pools, tok_doc, n_docs);
+        if (i2 < T) {
+            nxt = row_info(i2, pair_base, cu_seqlens, cu_pools, tok_doc, n_docs);
+            scores_ok(nxt);
+        }
         const bool cur_mid = mid_row(cur, topk);
         const bool pf_nxt = fast_row(nxt, topk);
-        if (pf_nxt && !cur_mid) prefetch_row(rowbuf + ((k + 1) & 1) * ROWBUF, scores, nxt.start, nxt.n);
+        if (pf_nxt && !cur_mid) {
+            const int upt = contig_upt(nxt.start, nxt.n);
+            if (upt) prefetch_row_contig(rowbuf + ((k + 1) & 1) * ROWBUF, scores, nxt.start, nxt.n, upt);
+            else prefetch_row(rowbuf + ((k + 1) & 1) * ROWBUF, scores, nxt.start, nxt.n);
+        }
         asm volatile("cp.async.commit_group;\n" ::: "memory");
 
         int32_t* row = indices + (int64_t)i * W;
-        const DocMap map{cur.s_d};
+        const DocMap map{cur.s_d, W, T, status};
         if (cur.d < 0) {
             for (int j = t; j < W; j += SEL_THREADS) row[j] = -1;
         } else if (cur.n <= topk) {                   // every candidate is kept: the causal prefix
@@ -474,10 +613,16 @@ __global__ void __launch_bounds__(SEL_THREADS, SEL_CTAS_PER_SM) select_kernel(co
             if (cur.n <= FAST_MAX) {
                 asm volatile("cp.async.wait_group 1;\n" ::: "memory");
                 __syncthreads();
-                const float* sc = rowbuf + (k & 1) * ROWBUF + (int)(cur.start & 3);
-                if (cur.n <= 8 * SEL_THREADS) select_registers<8>(s, sc, cur.n, topk, map, row);
-                else if (cur.n <= 16 * SEL_THREADS) select_registers<16>(s, sc, cur.n, topk, map, row);
-                else select_registers<32>(s, sc, cur.n, topk, map, row);
+                const float* bufk = rowbuf + (k & 1) * ROWBUF;
+                const int off = (int)(cur.start & 3);
+                switch (contig_upt(cur.start, cur.n)) {
+                    case 2: select_contig<2>(s, bufk, cur.n, off, topk, map, row); break;
+                    case 3: select_contig<3>(s, bufk, cur.n, off, topk, map, row); break;
+                    case 4: select_contig<4>(s, bufk, cur.n, off, topk, map, row); break;
+                    case 6: select_contig<6>(s, bufk, cur.n, off, topk, map, row); break;
+                    case 8: select_contig<8>(s, bufk, cur.n, off, topk, map, row); break;
+                    default: select_registers<32>(s, bufk + off, cur.n, topk, map, row); break;
+                }
             } else if (cur_mid) {                     // no copy is in flight: this row was not prefetched
                 prefetch_row(rowbuf, scores, cur.start, cur.n);
                 asm volatile("cp.async.commit_group;\n" ::: "memory");
@@ -562,7 +707,7 @@ int launch_select(const float* scores, const int64_t* pair_base, const kpool_lay
     }
     const int grid = L.T < SEL_CTAS_PER_SM * n_sm[dev] ? L.T : SEL_CTAS_PER_SM * n_sm[dev];
     select_kernel<<<grid, SEL_THREADS, kDyn, stream>>>(scores, pair_base, L.cu_seqlens, L.cu_pools, L.tok_doc,
-                                                      L.n_docs, L.T, topk, indices, W);
+                                                      L.n_docs, L.T, topk, indices, W, pairs_before(L.T), L.status);
     return cudaGetLastError() == cudaSuccess ? KPOOL_OK : KPOOL_ERR_CUDA;
 }
 

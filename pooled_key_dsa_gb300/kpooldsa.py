@@ -17,7 +17,8 @@ _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "li
 
 KPOOL_OK = 0
 ERRORS = {1: "KPOOL_ERR_INVALID_ARG", 2: "KPOOL_ERR_SHAPE", 3: "KPOOL_ERR_ALIGN", 4: "KPOOL_ERR_LAYOUT",
-          5: "KPOOL_ERR_INDEX_RANGE", 6: "KPOOL_ERR_TIMEOUT", 7: "KPOOL_ERR_CUDA", 8: "KPOOL_ERR_WORKSPACE"}
+          5: "KPOOL_ERR_INDEX_RANGE", 6: "KPOOL_ERR_TIMEOUT", 7: "KPOOL_ERR_CUDA", 8: "KPOOL_ERR_WORKSPACE",
+          9: "KPOOL_ERR_CHECK"}
 CODES = {v: k for k, v in ERRORS.items()}
 
 EXPORTED = ("kpool_workspace_bytes", "kpool_workspace_offsets", "kpool_build", "dsa_index", "sparse_mla_fwd",
@@ -70,6 +71,16 @@ class WsOffsets(ctypes.Structure):
 
 
 _lib = None
+_LIB_DEFAULT = _LIB_PATH
+_LIB_CHECKED = os.path.join(os.path.dirname(_LIB_PATH), "libkpooldsa_checked.so")
+
+
+def use_checked_library(on: bool) -> None:
+    """Switch the binding to the KPOOL_CHECKED build of the library (internal bounds checks that
+    record KPOOL_ERR_CHECK in the status word) or back to the default build; later calls load it."""
+    global _LIB_PATH, _lib
+    _LIB_PATH = _LIB_CHECKED if on else _LIB_DEFAULT
+    _lib = None
 
 
 def lib():

@@ -34,6 +34,16 @@ def test_every_declared_symbol_is_exported(lib):
     assert set(names) <= set(K.EXPORTED) | {n for n in names if hasattr(lib, n)}
 
 
+def test_checked_build_exports_the_same_symbols():
+    """The KPOOL_CHECKED build (internal bounds checks) links and exports every declared function."""
+    import ctypes as C
+    L = C.CDLL(B.build(checked=True))
+    for name in _declared_functions():
+        assert hasattr(L, name), name
+    L.kpool_strerror.restype = C.c_char_p
+    assert L.kpool_strerror(K.CODES["KPOOL_ERR_CHECK"]) == b"internal bounds check failed"
+
+
 def test_version_and_strerror(lib):
     assert "sm_103a" in K.version()
     for code in range(0, 9):
