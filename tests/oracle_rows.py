@@ -86,10 +86,30 @@ def _bf16_bits_to_f32(bits):
     return (np.asarray(bits, np.uint16).astype(np.uint32) << 16).view(np.float32)
 
 
+U32 = 2.0 ** -24          # unit roundoff of fp32
+
+
+def gamma(n: int) -> float:
+    """Bound on the relative error of an n-term fp32 sum (n u / (1 - n u))."""
+    return n * U32 / (1.0 - n * U32)
+
+
+def score_error_bound(qd_abs, kd_abs, ws_abs, sk, o_abs):
+    """Per-pool bound on |GPU score - oracle score| for one query row.  The E4M3 products are exact in fp32;
+    the GPU sums the d_i products of a head in fp32 (error <= gamma(d_i) * sum |q k|), takes ReLU (exact), sums
+    the H_i weighted heads in fp32 (error <= gamma(H_i + 2) * sum |ws| ReLU, and ReLU(x) <= sum |q k|), scales by
+    s_k (one rounding); the oracle's fp64 result is rounded to fp32 once.  So
+    |d| <= s_k * (gamma(d_i) + gamma(H_i + 2)) * sum_h |ws_h| A_hp + 2^-23 |S_p|, A_hp = sum_d |q_hd| |k_pd|."""
+    A = qd_abs @ kd_abs.T                                        # [H_i, n]
+    hi, di = qd_abs.shape
+    return sk * (gamma(di) + gamma(hi + 2)) * (ws_abs @ A) + 2.0 ** -23 * o_abs
+
+
 def check_chunk(task):
     """One chunk of rows: (rows, q_idx bf16 bits [n,H_i,d_i], GPU q8 [n,H_i,d_i], GPU ws [n,H_i], GPU scores
     (one array or None per row), GPU index rows [n,W]).  Returns the q8/ws mismatch counts, the worst score
-    error relative to the row's largest oracle score, and the row comparison counts."""
+    error relative to the row's largest oracle score, the worst ratio of a score's error to its own bound
+    (:func:`score_error_bound`), and the row comparison counts."""
     rows, qbits, q8_g, ws_g, sc_g, idx_g = task
     sh = _SHARED
     q8_o, sq_o = O.quantize_queries(_bf16_bits_to_f32(qbits))
@@ -97,15 +117,25 @@ def check_chunk(task):
     ws_o = (sh["w"][rows] * sq_o).astype(np.float32)
     ws_bad = int(np.count_nonzero(np.any(ws_o.view(np.uint32) != ws_g.view(np.uint32), axis=1)))
     S_o = O.scores_fp8(q8_o, sq_o, sh["k8"], sh["s_k"], sh["w"], sh["layout"], rows)
+    if "kd_abs" not in sh:
+        sh["kd_abs"] = np.abs(O.e4m3_decode(sh["k8"]))
     worst = 0.0
+    worst_bound = 0.0
     for n, g in enumerate(sc_g):
         if g is None:
             continue
         o = S_o[n].astype(np.float64)
         scale = max(np.abs(o).max(), 1e-30)
-        worst = max(worst, float(np.abs(g - o).max() / scale))
+        err = np.abs(np.asarray(g, np.float64) - o)
+        worst = max(worst, float(err.max() / scale))
+        d, _, n_i, _ = O.query_geometry(sh["layout"], int(rows[n]))
+        p0 = int(sh["layout"]["cu_pools"][d])
+        bound = score_error_bound(np.abs(O.e4m3_decode(q8_o[n])), sh["kd_abs"][p0:p0 + n_i],
+                                  np.abs(ws_o[n].astype(np.float64)),
+                                  np.asarray(sh["s_k"][p0:p0 + n_i], np.float64), np.abs(o))
+        worst_bound = max(worst_bound, float((err / np.maximum(bound, 1e-300)).max()))
     stats = compare_rows(idx_g, sh["layout"], rows, S_o, sh["topk"], sh["W"])
-    return {"q8_bad": q8_bad, "ws_bad": ws_bad, "worst": worst, "stats": stats}
+    return {"q8_bad": q8_bad, "ws_bad": ws_bad, "worst": worst, "worst_bound": worst_bound, "stats": stats}
 
 
 def check_rows(rows, qbits, q8_g, ws_g, scores_g, idx_g, shared, workers=None, chunk=256):
@@ -137,4 +167,5 @@ def check_rows(rows, qbits, q8_g, ws_g, scores_g, idx_g, shared, workers=None, c
                     os.environ[k] = v
     return {"q8_bad": sum(p["q8_bad"] for p in parts), "ws_bad": sum(p["ws_bad"] for p in parts),
             "worst": max((p["worst"] for p in parts), default=0.0),
+            "worst_bound": max((p["worst_bound"] for p in parts), default=0.0),
             "stats": merge_stats([p["stats"] for p in parts])}

@@ -65,9 +65,10 @@ def _parity_of(wl, rows=None, attn_rows=None, attention=True):
     KP.record(f"[{wl.name}] index rows: {st['rows']} checked ({'all' if len(rows) == wl.T else 'sample'} of "
               f"{wl.T}), {st['exact']} bit-exact, {st['boundary_rows']} boundary rows ({st['boundary_pools']} "
               f"pools), hard {st['hard']}; q8 rows off {chk['q8_bad']}, ws rows off {chk['ws_bad']}; "
-              f"score rel err {chk['worst']:.2e}")
+              f"score rel err {chk['worst']:.2e}, worst error / its per-pool bound {chk['worst_bound']:.2e}")
     assert chk["q8_bad"] == 0 and chk["ws_bad"] == 0
     assert chk["worst"] <= 1e-5, chk["worst"]
+    assert chk["worst_bound"] <= 1.0, chk["worst_bound"]
     assert st["hard"] == 0, st["hard_rows"][:10]
     if not attention:
         return wl, res
