@@ -225,18 +225,27 @@ typedef struct {
 #define KPOOL_MAX_CHUNKS 64
 
 /* Enqueues, for query rows cut into n_chunks (1..KPOOL_MAX_CHUNKS) blocks:
- *   s_in:      keys, indexer inputs and kv_lat to the device, then q_lat
- *              block by block;
- *   s_compute: kpool_build and dsa_index over all rows (after the inputs
- *              they read), then sparse_mla_fwd_rows block by block, each
- *              after its q_lat block has arrived;
+ *   s_in:      keys, gate, ape, kv_lat and w to the device, then each
+ *              block's q_idx and q_lat rows;
+ *   s_compute: kpool_build, then block by block, each after its rows have
+ *              arrived: the block's index rows (Hadamard/FP8 of its queries,
+ *              their scores, the select) and sparse_mla_fwd_rows;
  *   s_out:     out and lse of each block back to the host once its
  *              attention is done;
  * and makes s_compute wait for the last copy-out, so the forward is complete
- * when s_compute is.  The three streams must be distinct, non-default
- * streams for the copies to overlap.  Device errors go to layout->status;
- * host-side errors return before or between enqueues (work already
- * enqueued still runs).  Creates and releases 2*n_chunks+2 CUDA events. */
+ * when s_compute is.
+ * Blocks are indexed one at a time when the tcgen05 scorer serves the shape
+ * (d_idx = 128) and host->cu_seqlens starts at 0, never decreases and ends
+ * at T. The host reads host->cu_seqlens to place each block edge on the start
+ * of a scoring query group (256 / n_idx_heads rows from each document's
+ * start), so blocks are near, not exactly, T / n_chunks rows. Otherwise the
+ * whole dsa_index runs after all of q_idx has arrived, and blocks are
+ * ceil(T / n_chunks) rows. Either way the results are those of kpool_build,
+ * dsa_index and sparse_mla_fwd.
+ * The three streams must be distinct, non-default streams for the copies to
+ * overlap. Device errors go to layout->status. Host-side errors return before
+ * or between enqueues (work already enqueued still runs). Creates and
+ * releases 2*n_chunks+2 CUDA events. */
 int kpool_forward_host(const kpool_host_io* host, const kpool_dev_io* dev, int32_t n_docs, int32_t T,
                        const kpool_params* p, int32_t n_chunks, kpool_stream_t s_in,
                        kpool_stream_t s_compute, kpool_stream_t s_out);

@@ -59,6 +59,112 @@ static bool layout_ok(const kpool_layout* L) {
            L->pool_tok_start && L->tok_doc && L->status;
 }
 
+// The buffers and shapes of one dsa_index call, checked once; its stages run whole (dsa_index) or per
+// block of query rows (the host-buffer forward).
+struct IndexPlan {
+    const void* q_idx;
+    const float* w;
+    const float* kpool;
+    kpool_layout L;
+    const kpool_params* p;
+    int topk, W, T, qg;
+    int32_t* indices;
+    uint8_t* q8;
+    float* ws;
+    uint8_t* k8;
+    float* s_k;
+    int64_t* pair_base;
+    int32_t* sched;
+    float* scores;
+};
+
+static int index_plan(const void* q_idx, const float* w, const float* kpool, const kpool_layout* layout, int32_t topk,
+                      const kpool_params* p, void* workspace, size_t workspace_bytes, int32_t* indices, int32_t W,
+                      IndexPlan* out) {
+    if (!params_ok(p) || !layout_ok(layout)) return KPOOL_ERR_INVALID_ARG;
+    const int tk = topk > 0 ? topk : p->topk;
+    const int T = layout->T;
+    if (T > 0 && (!q_idx || !w || !kpool || !indices)) return KPOOL_ERR_INVALID_ARG;
+    if ((int64_t)W < (int64_t)KPOOL * tk + KPOOL - 1 || W % 4 != 0) return KPOOL_ERR_SHAPE;
+    if (!aligned(q_idx, 8) || !aligned(kpool, 16) || !aligned(indices, 16) || !aligned(workspace, 256))
+        return KPOOL_ERR_ALIGN;
+    const WsLayout wl = ws_layout(T, layout->n_docs, T / KPOOL, p->n_idx_heads, p->d_idx);
+    if (!workspace || workspace_bytes < wl.total) return KPOOL_ERR_WORKSPACE;
+    IndexPlan& P = *out;
+    P.q_idx = q_idx;
+    P.w = w;
+    P.kpool = kpool;
+    P.L = *layout;
+    P.L.max_pools = T / KPOOL;     // every split of T tokens has at most floor(T/4) pools
+    P.p = p;
+    P.topk = tk;
+    P.W = W;
+    P.T = T;
+    P.qg = scoring_group(p->n_idx_heads, p->d_idx);
+    P.indices = indices;
+    uint8_t* base = static_cast<uint8_t*>(workspace);
+    P.q8 = base + wl.q8;
+    P.ws = reinterpret_cast<float*>(base + wl.ws);
+    P.k8 = base + wl.k8;
+    P.s_k = reinterpret_cast<float*>(base + wl.s_k);
+    P.pair_base = reinterpret_cast<int64_t*>(base + wl.pair_base);
+    P.sched = reinterpret_cast<int32_t*>(base + wl.sched);
+    P.scores = reinterpret_cast<float*>(base + wl.scores);
+    return KPOOL_OK;
+}
+
+// Per-document score bases and work schedule, and the pooled keys' Hadamard/FP8.
+static int index_setup(const IndexPlan& P, cudaStream_t s) {
+    int rc = launch_index_prep(P.L, P.topk, P.qg, P.pair_base, P.sched, s);
+    if (rc != KPOOL_OK) return rc;
+    return launch_hadamard_fp8(P.kpool, false, P.L.max_pools, P.p->d_idx, P.L.cu_pools + P.L.n_docs, nullptr, P.k8,
+                               P.s_k, nullptr, s);
+}
+
+// Query rows r0 .. r1-1: Hadamard/FP8 of their queries and head weights.
+static int index_queries(const IndexPlan& P, int r0, int r1, cudaStream_t s) {
+    const int64_t hv = (int64_t)P.p->n_idx_heads, e = hv * P.p->d_idx;
+    return launch_hadamard_fp8(static_cast<const uint16_t*>(P.q_idx) + r0 * e, true, (int64_t)(r1 - r0) * hv,
+                               P.p->d_idx, nullptr, P.w + r0 * hv, P.q8 + r0 * e, nullptr, P.ws + r0 * hv, s);
+}
+
+// Work items of the tcgen05 scoring schedule whose first query row lies below row R: documents in order,
+// each with the groups of qg queries from the group holding r = 4*topk + 3 (the numbering of the schedule
+// kernel), counted on the host from the host copy of cu_seqlens.
+static int items_before(const int32_t* cu, int n_docs, int topk, int qg, int R) {
+    int64_t acc = 0;
+    const int q0 = (KPOOL * topk + KPOOL - 1) / qg;
+    for (int d = 0; d < n_docs; ++d) {
+        const int s = cu[d], L = cu[d + 1] - cu[d];
+        if (R <= s) break;
+        const int q_all = (L + qg - 1) / qg;
+        const int n_d = q_all > q0 ? q_all - q0 : 0;
+        if (R >= s + L) {
+            acc += n_d;
+            continue;
+        }
+        const int c = (R - s + qg - 1) / qg - q0;     // groups (q0 + k) * qg < R - s
+        acc += c < 0 ? 0 : (c > n_d ? n_d : c);
+        break;
+    }
+    return (int)acc;
+}
+
+// Row R moved down to the start of its document's query group (groups of qg rows from each document's start).
+static int group_floor(const int32_t* cu, int n_docs, int qg, int R) {
+    for (int d = 0; d < n_docs; ++d)
+        if (R < cu[d + 1]) return cu[d] + (R - cu[d]) / qg * qg;
+    return R;
+}
+
+// A host copy of cu_seqlens fit for planning row blocks: starts at 0, never decreases, ends at T.
+static bool host_cu_ok(const int32_t* cu, int n_docs, int T) {
+    if (!cu || cu[0] != 0 || cu[n_docs] != T) return false;
+    for (int d = 0; d < n_docs; ++d)
+        if (cu[d + 1] < cu[d]) return false;
+    return true;
+}
+
 }  // namespace kpool
 
 using namespace kpool;
@@ -100,42 +206,19 @@ int dsa_index(const void* q_idx, const float* w, const float* kpool, const kpool
               const kpool_params* p, void* workspace, size_t workspace_bytes, int32_t* indices, int32_t W,
               kpool_stream_t stream) {
     const Range range("dsa_index");
-    if (!params_ok(p) || !layout_ok(layout)) return KPOOL_ERR_INVALID_ARG;
-    const int tk = topk > 0 ? topk : p->topk;
-    const int T = layout->T;
-    if (T > 0 && (!q_idx || !w || !kpool || !indices)) return KPOOL_ERR_INVALID_ARG;
-    if ((int64_t)W < (int64_t)KPOOL * tk + KPOOL - 1 || W % 4 != 0) return KPOOL_ERR_SHAPE;
-    if (!aligned(q_idx, 8) || !aligned(kpool, 16) || !aligned(indices, 16) || !aligned(workspace, 256))
-        return KPOOL_ERR_ALIGN;
-    const WsLayout wl = ws_layout(T, layout->n_docs, T / KPOOL, p->n_idx_heads, p->d_idx);
-    if (!workspace || workspace_bytes < wl.total) return KPOOL_ERR_WORKSPACE;
-    kpool_layout L = *layout;
-    L.max_pools = T / KPOOL;       // every split of T tokens has at most floor(T/4) pools
+    IndexPlan P;
+    int rc = index_plan(q_idx, w, kpool, layout, topk, p, workspace, workspace_bytes, indices, W, &P);
+    if (rc != KPOOL_OK) return rc;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    uint8_t* base = static_cast<uint8_t*>(workspace);
-    uint8_t* q8 = base + wl.q8;
-    float* ws = reinterpret_cast<float*>(base + wl.ws);
-    uint8_t* k8 = base + wl.k8;
-    float* s_k = reinterpret_cast<float*>(base + wl.s_k);
-    int64_t* pair_base = reinterpret_cast<int64_t*>(base + wl.pair_base);
-    int32_t* sched = reinterpret_cast<int32_t*>(base + wl.sched);
-    float* scores = reinterpret_cast<float*>(base + wl.scores);
-    int rc;
     if ((rc = stage_mark(0, s)) != KPOOL_OK) return rc;
-    if ((rc = launch_index_prep(L, tk, scoring_group(p->n_idx_heads, p->d_idx), pair_base, sched, s)) != KPOOL_OK)
-        return rc;
-    if ((rc = launch_hadamard_fp8(q_idx, true, (int64_t)T * p->n_idx_heads, p->d_idx, nullptr, w, q8, nullptr, ws,
-                                  s)) != KPOOL_OK)
-        return rc;
-    if ((rc = launch_hadamard_fp8(kpool, false, L.max_pools, p->d_idx, L.cu_pools + L.n_docs, nullptr, k8, s_k,
-                                  nullptr, s)) != KPOOL_OK)
-        return rc;
+    if ((rc = index_setup(P, s)) != KPOOL_OK) return rc;
+    if ((rc = index_queries(P, 0, P.T, s)) != KPOOL_OK) return rc;
     if ((rc = stage_mark(1, s)) != KPOOL_OK) return rc;
-    if ((rc = launch_score(q8, ws, k8, s_k, L, pair_base, sched, tk, p->n_idx_heads, p->d_idx, scores, s)) !=
-        KPOOL_OK)
+    if ((rc = launch_score(P.q8, P.ws, P.k8, P.s_k, P.L, P.pair_base, P.sched, P.topk, p->n_idx_heads, p->d_idx,
+                           P.scores, s)) != KPOOL_OK)
         return rc;
     if ((rc = stage_mark(2, s)) != KPOOL_OK) return rc;
-    if ((rc = launch_select(scores, pair_base, L, tk, indices, W, s)) != KPOOL_OK) return rc;
+    if ((rc = launch_select(P.scores, P.pair_base, P.L, P.topk, P.indices, P.W, s)) != KPOOL_OK) return rc;
     return stage_mark(3, s);
 }
 
@@ -304,72 +387,103 @@ int kpool_forward_host(const kpool_host_io* h, const kpool_dev_io* d, int32_t n_
     if (d->layout->cu_seqlens != d->cu_seqlens || d->layout->T != T || d->layout->n_docs != n_docs)
         return KPOOL_ERR_INVALID_ARG;
     if (p->d_lat != D_LAT || p->kpool != KPOOL || p->n_heads < 1 || p->n_heads > 64) return KPOOL_ERR_SHAPE;
+    IndexPlan P;
+    int rc = index_plan(d->q_idx, d->w, d->kpool, d->layout, p->topk, p, d->workspace, d->workspace_bytes,
+                        d->indices, d->W, &P);
+    if (rc != KPOOL_OK) return rc;
     cudaStream_t si = reinterpret_cast<cudaStream_t>(s_in), sc = reinterpret_cast<cudaStream_t>(s_compute),
                  so = reinterpret_cast<cudaStream_t>(s_out);
     const size_t q_row = (size_t)p->n_heads * D_LAT * 2;       // bytes of one q_lat / out row
     const size_t lse_row = (size_t)p->n_heads * 4;
+    const size_t qi_row = (size_t)p->n_idx_heads * p->d_idx * 2;
+    const size_t w_row = (size_t)p->n_idx_heads * 4;
+    // Query-row blocks.  With the tcgen05 scorer and a well-formed host cu_seqlens, each block is indexed
+    // on its own (its queries' Hadamard/FP8, scores, select) as soon as its q_idx rows have arrived, so
+    // the first attention block and the first copy-out start early; block edges then fall on the
+    // scorer's query groups, so no work item spans two blocks.  Otherwise the indexer runs over all
+    // rows before the first attention block.
+    const bool blocked = P.qg > 0 && host_cu_ok(h->cu_seqlens, n_docs, T);
+    int32_t edge[KPOOL_MAX_CHUNKS + 1];
     const int32_t rows_per = (T + n_chunks - 1) / n_chunks;
     n_chunks = (T + rows_per - 1) / rows_per;
+    edge[0] = 0;
+    for (int c = 1; c < n_chunks; ++c)
+        edge[c] = blocked ? group_floor(h->cu_seqlens, n_docs, P.qg, c * rows_per) : c * rows_per;
+    edge[n_chunks] = T;
 
     cudaEvent_t ev[2 * KPOOL_MAX_CHUNKS + 2];
     const int n_ev = 2 * n_chunks + 2;
-    int made = 0, rc = KPOOL_OK;
+    int made = 0;
     for (; made < n_ev; ++made)
         if (cudaEventCreateWithFlags(&ev[made], cudaEventDisableTiming) != cudaSuccess) { rc = KPOOL_ERR_CUDA; break; }
     cudaEvent_t ev_in = ev[0], ev_out = ev[1];
     cudaEvent_t* ev_q = ev + 2;
     cudaEvent_t* ev_mla = ev + 2 + n_chunks;
     auto h2d = [&](void* dst, const void* src, size_t bytes) {
-        if (rc == KPOOL_OK && cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, si) != cudaSuccess)
+        if (rc == KPOOL_OK && bytes > 0 && cudaMemcpyAsync(dst, src, bytes, cudaMemcpyHostToDevice, si) != cudaSuccess)
             rc = KPOOL_ERR_CUDA;
     };
     auto d2h = [&](void* dst, const void* src, size_t bytes) {
-        if (rc == KPOOL_OK && cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToHost, so) != cudaSuccess)
+        if (rc == KPOOL_OK && bytes > 0 && cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToHost, so) != cudaSuccess)
             rc = KPOOL_ERR_CUDA;
     };
     auto ok = [&](cudaError_t e) {
         if (rc == KPOOL_OK && e != cudaSuccess) rc = KPOOL_ERR_CUDA;
     };
-    // copy-in stream: keys and indexer inputs, then the query rows chunk by chunk
+    auto rows_of = [](void* base, size_t row, int32_t r0) { return static_cast<uint8_t*>(base) + r0 * row; };
+    auto crows_of = [](const void* base, size_t row, int32_t r0) { return static_cast<const uint8_t*>(base) + r0 * row; };
+    // copy-in stream: keys and what every block shares, then each block's query rows
     h2d(d->cu_seqlens, h->cu_seqlens, (size_t)(n_docs + 1) * 4);
     h2d(d->k, h->k, (size_t)T * p->d_idx * 2);
     h2d(d->gate, h->gate, (size_t)T * p->d_idx * 4);
     h2d(d->ape, h->ape, (size_t)KPOOL * p->d_idx * 4);
     h2d(d->kv_lat, h->kv_lat, (size_t)T * D_LAT * 2);
-    h2d(d->q_idx, h->q_idx, (size_t)T * p->n_idx_heads * p->d_idx * 2);
-    h2d(d->w, h->w, (size_t)T * p->n_idx_heads * 4);
+    h2d(d->w, h->w, (size_t)T * w_row);
+    if (!blocked) h2d(d->q_idx, h->q_idx, (size_t)T * qi_row);
     if (rc == KPOOL_OK) ok(cudaEventRecord(ev_in, si));
     for (int c = 0; c < n_chunks && rc == KPOOL_OK; ++c) {
-        const int32_t r0 = c * rows_per, n = (T - r0 < rows_per) ? T - r0 : rows_per;
-        h2d(static_cast<uint8_t*>(d->q_lat) + r0 * q_row, static_cast<const uint8_t*>(h->q_lat) + r0 * q_row,
-            (size_t)n * q_row);
+        const int32_t r0 = edge[c], n = edge[c + 1] - edge[c];
+        if (blocked) h2d(rows_of(d->q_idx, qi_row, r0), crows_of(h->q_idx, qi_row, r0), (size_t)n * qi_row);
+        h2d(rows_of(d->q_lat, q_row, r0), crows_of(h->q_lat, q_row, r0), (size_t)n * q_row);
         if (rc == KPOOL_OK) ok(cudaEventRecord(ev_q[c], si));
     }
-    // compute stream: indexer over all rows, then attention chunk by chunk
+    // compute stream: pooled keys and the index schedule, then block by block (index rows when blocked)
+    // and attention
     if (rc == KPOOL_OK) ok(cudaStreamWaitEvent(sc, ev_in, 0));
     if (rc == KPOOL_OK)
         rc = kpool_build(d->k, d->gate, d->ape, d->cu_seqlens, n_docs, T, p, d->kpool, d->layout, s_compute);
-    if (rc == KPOOL_OK)
-        rc = dsa_index(d->q_idx, d->w, d->kpool, d->layout, p->topk, p, d->workspace, d->workspace_bytes,
-                       d->indices, d->W, s_compute);
+    if (rc == KPOOL_OK) {
+        if (blocked)
+            rc = index_setup(P, sc);
+        else
+            rc = dsa_index(d->q_idx, d->w, d->kpool, d->layout, p->topk, p, d->workspace, d->workspace_bytes,
+                           d->indices, d->W, s_compute);
+    }
     for (int c = 0; c < n_chunks && rc == KPOOL_OK; ++c) {
-        const int32_t r0 = c * rows_per, n = (T - r0 < rows_per) ? T - r0 : rows_per;
+        const int32_t r0 = edge[c], r1 = edge[c + 1], n = r1 - r0;
         ok(cudaStreamWaitEvent(sc, ev_q[c], 0));
-        if (rc == KPOOL_OK)
-            rc = sparse_mla_fwd_rows(static_cast<const uint8_t*>(d->q_lat) + r0 * q_row, d->kv_lat,
-                                     d->indices + (size_t)r0 * d->W, d->W, n, T, p->n_heads, p->scale,
-                                     static_cast<uint8_t*>(d->out) + r0 * q_row, d->lse + (size_t)r0 * p->n_heads,
-                                     d->layout->status, s_compute);
+        if (blocked && rc == KPOOL_OK && n > 0) {
+            rc = index_queries(P, r0, r1, sc);
+            if (rc == KPOOL_OK) {
+                const int j0 = items_before(h->cu_seqlens, n_docs, P.topk, P.qg, r0);
+                const int j1 = items_before(h->cu_seqlens, n_docs, P.topk, P.qg, r1);
+                rc = launch_score(P.q8, P.ws, P.k8, P.s_k, P.L, P.pair_base, P.sched, P.topk, p->n_idx_heads,
+                                  p->d_idx, P.scores, sc, j0, j1);
+            }
+            if (rc == KPOOL_OK) rc = launch_select(P.scores, P.pair_base, P.L, P.topk, P.indices, P.W, sc, r0, r1);
+        }
+        if (rc == KPOOL_OK && n > 0)
+            rc = sparse_mla_fwd_rows(crows_of(d->q_lat, q_row, r0), d->kv_lat, d->indices + (size_t)r0 * d->W, d->W,
+                                     n, T, p->n_heads, p->scale, rows_of(d->out, q_row, r0),
+                                     d->lse + (size_t)r0 * p->n_heads, d->layout->status, s_compute);
         if (rc == KPOOL_OK) ok(cudaEventRecord(ev_mla[c], sc));
     }
-    // copy-out stream: each chunk's results as soon as its attention is done
+    // copy-out stream: each block's results as soon as its attention is done
     for (int c = 0; c < n_chunks && rc == KPOOL_OK; ++c) {
-        const int32_t r0 = c * rows_per, n = (T - r0 < rows_per) ? T - r0 : rows_per;
+        const int32_t r0 = edge[c], n = edge[c + 1] - edge[c];
         ok(cudaStreamWaitEvent(so, ev_mla[c], 0));
-        d2h(static_cast<uint8_t*>(h->out) + r0 * q_row, static_cast<const uint8_t*>(d->out) + r0 * q_row,
-            (size_t)n * q_row);
-        d2h(reinterpret_cast<uint8_t*>(h->lse) + r0 * lse_row,
-            reinterpret_cast<const uint8_t*>(d->lse) + r0 * lse_row, (size_t)n * lse_row);
+        d2h(rows_of(h->out, q_row, r0), crows_of(d->out, q_row, r0), (size_t)n * q_row);
+        d2h(rows_of(h->lse, lse_row, r0), crows_of(d->lse, lse_row, r0), (size_t)n * lse_row);
     }
     // the compute stream ends after the last copy-out
     if (rc == KPOOL_OK) ok(cudaEventRecord(ev_out, so));
@@ -420,6 +534,6 @@ const char* kpool_strerror(int code) {
 
 // The tags after the arch name identify the kernel generations (used to match
 // stored profiler counters to the code that produced them).
-const char* kpool_version(void) { return "kpooldsa 0.16 sm_103a mla-tc11 score-tc3 select5 proj1 bwd4 decode2 pool2 hadamard3"; }
+const char* kpool_version(void) { return "kpooldsa 0.17 sm_103a mla-tc11 score-tc3 select5 proj1 bwd4 decode2 pool2 hadamard3"; }
 
 }  // extern "C"

@@ -35,19 +35,21 @@ int launch_index_prep(const kpool_layout& L, int topk, int qg, int64_t* pair_bas
 // 128), or 0 when the mma.sync kernel serves the shape (d_i = 64).
 int scoring_group(int n_idx_heads, int d_idx);
 
-// FP8 pool scores into the compact triangle.
+// FP8 pool scores into the compact triangle, for the work items j_lo .. j_hi-1 of the schedule
+// (j_hi < 0: every item from j_lo on; item ranges other than the whole schedule need the tcgen05 kernel).
 int launch_score(const uint8_t* q8, const float* ws, const uint8_t* k8, const float* s_k, const kpool_layout& L,
                  const int64_t* pair_base, const int32_t* sched, int topk, int n_idx_heads, int d_idx,
-                 float* scores, cudaStream_t stream);
+                 float* scores, cudaStream_t stream, int j_lo = 0, int j_hi = -1);
 
 // The mma.sync e4m3 scoring kernel (d_i = 64 shapes).
 int launch_score_mma(const uint8_t* q8, const float* ws, const uint8_t* k8, const float* s_k, const kpool_layout& L,
                      const int64_t* pair_base, const int32_t* sched, int topk, int n_idx_heads, int d_idx,
                      float* scores, cudaStream_t stream);
 
-// Top-k select, expansion to positions, own tail, -1 padding.
+// Top-k select, expansion to positions, own tail, -1 padding, for the query rows row0 .. row1-1
+// (row1 < 0: to the last row).
 int launch_select(const float* scores, const int64_t* pair_base, const kpool_layout& L, int topk, int32_t* indices,
-                  int W, cudaStream_t stream);
+                  int W, cudaStream_t stream, int row0 = 0, int row1 = -1);
 
 int launch_sparse_mla(const uint16_t* q_lat, const uint16_t* kv_lat, const int32_t* indices, int W, int n_rows,
                       int T, int n_heads, float scale, uint16_t* out, float* lse, int32_t* status,

@@ -157,7 +157,7 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_tc_kernel(
     const float* __restrict__ s_k, const int32_t* __restrict__ cu_seqlens, const int32_t* __restrict__ cu_pools,
     int n_docs, int max_pools, int T, const int64_t* __restrict__ pair_base, const int32_t* __restrict__ sched,
     int topk, uint32_t b_box_bytes, uint32_t a_box_bytes, float* __restrict__ scores, int64_t n_scores,
-    int32_t* status) {
+    int32_t* status, int j_lo, int j_hi) {
     constexpr int QG = 256 / HI;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = smem_raw + ((1024u - (tc::smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -165,7 +165,8 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_tc_kernel(
     const uint32_t s_base = tc::smem_u32(smem);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     volatile int* abort_flag = &sm.abort;
-    const int total = sched[n_docs];
+    // work items j_lo .. j_hi-1 of the schedule (j_hi < 0: to the last item)
+    const int total = (j_hi < 0 ? sched[n_docs] : j_hi) - j_lo;
 
     if (tid == 0) {
         for (int b = 0; b < 2; ++b) {
@@ -197,8 +198,9 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_tc_kernel(
             // bounded waits of every role run out
             bool ok = g_score_tc_stall == 0 || tc::mbar_wait(tc::smem_u32(&sm.never), 0, abort_flag);
             for (int k = 0; ok; ++k, ++ni) {
-                const int j = item_of(k);
-                if (j >= total) break;
+                const int jj = item_of(k);
+                if (jj >= total) break;
+                const int j = j_lo + jj;
                 const Item it = decode_item(j, sched, cu_seqlens, cu_pools, n_docs, topk, QG);
                 const int ib = ni & 1;
                 if (!tc::mbar_wait(tc::smem_u32(&sm.b_empty[ib]), ((ni >> 1) & 1) ^ 1, abort_flag)) { ok = false; break; }
@@ -239,8 +241,9 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_tc_kernel(
             uint32_t ni = 0, na = 0, nacc = 0;
             bool ok = true;
             for (int k = 0; ok && !*abort_flag; ++k, ++ni) {
-                const int j = item_of(k);
-                if (j >= total) break;
+                const int jj = item_of(k);
+                if (jj >= total) break;
+                const int j = j_lo + jj;
                 const Item it = decode_item(j, sched, cu_seqlens, cu_pools, n_docs, topk, QG);
                 const int ib = ni & 1;
                 if (!tc::mbar_wait(tc::smem_u32(&sm.b_full[ib]), (ni >> 1) & 1, abort_flag)) { ok = false; break; }
@@ -285,8 +288,9 @@ __global__ void __launch_bounds__(SC_THREADS, 1) score_tc_kernel(
         uint32_t ni = 0, nacc = 0;
         bool bad = false;
         for (int k = 0;; ++k, ++ni) {
-            const int j = item_of(k);
-            if (j >= total) break;
+            const int jj = item_of(k);
+            if (jj >= total) break;
+            const int j = j_lo + jj;
             const Item it = decode_item(j, sched, cu_seqlens, cu_pools, n_docs, topk, QG);
             const int i0 = it.s_d + it.r0;
             // the item's head weights (256 floats), halved, into this group's shared buffer
@@ -405,7 +409,8 @@ static bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t b
 
 template <int HI>
 static int launch_tc(const uint8_t* q8, const float* ws, const uint8_t* k8, const float* s_k, const kpool_layout& L,
-                     const int64_t* pair_base, const int32_t* sched, int topk, float* scores, cudaStream_t stream) {
+                     const int64_t* pair_base, const int32_t* sched, int topk, float* scores, int j_lo, int j_hi,
+                     cudaStream_t stream) {
     static int n_sm[64] = {0};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return KPOOL_ERR_CUDA;
@@ -425,22 +430,26 @@ static int launch_tc(const uint8_t* q8, const float* ws, const uint8_t* k8, cons
     if (!make_map(&mq, q8, q_rows, b_rows) || !make_map(&mk, k8, k_rows, a_rows)) return KPOOL_ERR_CUDA;
     score_tc_kernel<HI><<<n_sm[dev], SC_THREADS, SC_SMEM, stream>>>(
         mq, mk, ws, s_k, L.cu_seqlens, L.cu_pools, L.n_docs, L.max_pools, L.T, pair_base, sched, topk, b_rows * 128,
-        a_rows * 128, scores, pairs_before(L.T), L.status);
+        a_rows * 128, scores, pairs_before(L.T), L.status, j_lo, j_hi);
     return cudaGetLastError() == cudaSuccess ? KPOOL_OK : KPOOL_ERR_CUDA;
 }
 
 int launch_score(const uint8_t* q8, const float* ws, const uint8_t* k8, const float* s_k, const kpool_layout& L,
                  const int64_t* pair_base, const int32_t* sched, int topk, int n_idx_heads, int d_idx,
-                 float* scores, cudaStream_t stream) {
+                 float* scores, cudaStream_t stream, int j_lo, int j_hi) {
     if (L.T <= 0) return KPOOL_OK;
-    if (scoring_group(n_idx_heads, d_idx) == 0)
+    if (scoring_group(n_idx_heads, d_idx) == 0) {
+        if (j_lo != 0 || j_hi >= 0) return KPOOL_ERR_SHAPE;        // item ranges are a tcgen05-kernel feature
         return launch_score_mma(q8, ws, k8, s_k, L, pair_base, sched, topk, n_idx_heads, d_idx, scores, stream);
+    }
+    if (j_lo < 0 || (j_hi >= 0 && j_hi < j_lo)) return KPOOL_ERR_INVALID_ARG;
+    if (j_hi >= 0 && j_hi == j_lo) return KPOOL_OK;
     switch (n_idx_heads) {
-        case 4: return launch_tc<4>(q8, ws, k8, s_k, L, pair_base, sched, topk, scores, stream);
-        case 8: return launch_tc<8>(q8, ws, k8, s_k, L, pair_base, sched, topk, scores, stream);
-        case 16: return launch_tc<16>(q8, ws, k8, s_k, L, pair_base, sched, topk, scores, stream);
-        case 32: return launch_tc<32>(q8, ws, k8, s_k, L, pair_base, sched, topk, scores, stream);
-        case 64: return launch_tc<64>(q8, ws, k8, s_k, L, pair_base, sched, topk, scores, stream);
+        case 4: return launch_tc<4>(q8, ws, k8, s_k, L, pair_base, sched, topk, scores, j_lo, j_hi, stream);
+        case 8: return launch_tc<8>(q8, ws, k8, s_k, L, pair_base, sched, topk, scores, j_lo, j_hi, stream);
+        case 16: return launch_tc<16>(q8, ws, k8, s_k, L, pair_base, sched, topk, scores, j_lo, j_hi, stream);
+        case 32: return launch_tc<32>(q8, ws, k8, s_k, L, pair_base, sched, topk, scores, j_lo, j_hi, stream);
+        case 64: return launch_tc<64>(q8, ws, k8, s_k, L, pair_base, sched, topk, scores, j_lo, j_hi, stream);
         default: return KPOOL_ERR_SHAPE;
     }
 }

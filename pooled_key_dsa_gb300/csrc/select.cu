@@ -556,7 +556,7 @@ __device__ __forceinline__ bool mid_row(const RowInfo& ri, int topk) {
 
 constexpr int SEL_CTAS_PER_SM = 3;                   // 3 x (65.6 KB row buffers + 8.2 KB) of shared memory
 
-// Persistent: block b walks rows b, b + gridDim.x, ...; the scores of the
+// Persistent: block b walks rows row0 + b, row0 + b + gridDim.x, ... below row1; the scores of the
 // next row are copied into shared memory (cp.async) while the current row is
 // ranked, so the load latency of a row is hidden behind the previous one.
 // A row longer than one row buffer but not two is copied into both when its
@@ -568,12 +568,13 @@ __global__ void __launch_bounds__(SEL_THREADS, SEL_CTAS_PER_SM) select_kernel(co
                                                              const int32_t* __restrict__ cu_pools,
                                                              const int32_t* __restrict__ tok_doc, int n_docs, int T,
                                                              int topk, int32_t* __restrict__ indices, int W,
-                                                             int64_t n_scores, int32_t* status) {
+                                                             int64_t n_scores, int32_t* status, int row0,
+                                                             int row1) {
     __shared__ SelectSmem s;
     extern __shared__ __align__(16) float rowbuf[];   // 2 x ROWBUF
     const int t = threadIdx.x;
-    int i = blockIdx.x;
-    if (i >= T) return;
+    int i = row0 + (int)blockIdx.x;                   // rows row0 .. row1-1 (row1 <= T)
+    if (i >= row1) return;
     // checked build: a row whose scores would fall outside the score triangle is left empty
     auto scores_ok = [&](RowInfo& ri) {
         if (ri.d >= 0 && ri.n > topk && !in_bounds(ri.start >= 0 && ri.start + ri.n <= n_scores, status)) ri.d = -1;
@@ -586,11 +587,11 @@ __global__ void __launch_bounds__(SEL_THREADS, SEL_CTAS_PER_SM) select_kernel(co
         else prefetch_row(rowbuf, scores, cur.start, cur.n);
     }
     asm volatile("cp.async.commit_group;\n" ::: "memory");
-    for (int k = 0; i < T; ++k, i += gridDim.x) {
+    for (int k = 0; i < row1; ++k, i += gridDim.x) {
         const int i2 = i + (int)gridDim.x;
         RowInfo nxt;
         nxt.d = -1;
-        if (i2 < T) {
+        if (i2 < row1) {
             nxt = row_info(i2, pair_base, cu_seqlens, cu_pools, tok_doc, n_docs);
             scores_ok(nxt);
         }
@@ -689,8 +690,10 @@ int launch_decode_select(const float* scores, int64_t stride, const int32_t* seq
 }
 
 int launch_select(const float* scores, const int64_t* pair_base, const kpool_layout& L, int topk, int32_t* indices,
-                  int W, cudaStream_t stream) {
-    if (L.T <= 0) return KPOOL_OK;
+                  int W, cudaStream_t stream, int row0, int row1) {
+    if (row1 < 0 || row1 > L.T) row1 = L.T;
+    if (row0 < 0) return KPOOL_ERR_INVALID_ARG;
+    if (row0 >= row1) return KPOOL_OK;
     constexpr int kDyn = 2 * ROWBUF * (int)sizeof(float);
     static int n_sm[64] = {0};
     int dev = 0;
@@ -705,9 +708,11 @@ int launch_select(const float* scores, const int64_t* pair_base, const kpool_lay
         if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return KPOOL_ERR_CUDA;
         n_sm[dev] = sms;
     }
-    const int grid = L.T < SEL_CTAS_PER_SM * n_sm[dev] ? L.T : SEL_CTAS_PER_SM * n_sm[dev];
+    const int n = row1 - row0;
+    const int grid = n < SEL_CTAS_PER_SM * n_sm[dev] ? n : SEL_CTAS_PER_SM * n_sm[dev];
     select_kernel<<<grid, SEL_THREADS, kDyn, stream>>>(scores, pair_base, L.cu_seqlens, L.cu_pools, L.tok_doc,
-                                                      L.n_docs, L.T, topk, indices, W, pairs_before(L.T), L.status);
+                                                      L.n_docs, L.T, topk, indices, W, pairs_before(L.T), L.status,
+                                                      row0, row1);
     return cudaGetLastError() == cudaSuccess ? KPOOL_OK : KPOOL_ERR_CUDA;
 }
 

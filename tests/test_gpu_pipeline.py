@@ -49,9 +49,19 @@ def test_row_blocks_give_the_unsplit_attention():
     assert torch.equal(lse_b, lse)
 
 
-@pytest.mark.parametrize("cfg,n_chunks", [(0, 3), (2, 5)])
+# Block counts and workloads: config 0 (d_i = 64) runs the whole indexer before the blocks; the others index
+# block by block, with block edges inside documents, blocks of a few query groups (64 blocks), one block, and
+# a packed set of tiny documents (no scored rows) beside documents past the scoring cutover (topk 64 pools).
+MIXED = ("mixed_docs", 37, (3, 5, 700, 9, 2051, 2060, 1), 64)
+
+
+@pytest.mark.parametrize("cfg,n_chunks", [(0, 3), (2, 5), (2, 64), (1, 1), (1, 16), (MIXED, 7), (MIXED, 37)])
 def test_host_pipeline_matches_the_device_path_and_the_oracle(cfg, n_chunks):
-    wl = workloads.workload(cfg)
+    if isinstance(cfg, tuple):
+        name, seed, lens, topk = cfg
+        wl = workloads.custom(name, seed, lens, topk=topk)
+    else:
+        wl = workloads.workload(cfg)
     inp = workloads.all_inputs(wl)
     d = KP.to_dev(inp)
     idx, out, lse = _device_path(wl, d)
