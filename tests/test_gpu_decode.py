@@ -156,3 +156,50 @@ def test_decode_guards():
     K.decode_index(inp.q_idx.cuda(), torch.from_numpy(inp.w).cuda(), k8, sk, torch.from_numpy(bad).cuda(),
                    torch.tensor(dw.seq_lens, dtype=torch.int32, device="cuda"), dw.topk, p, dw.W, status=st)
     assert K.check_status(st) == K.CODES["KPOOL_ERR_INDEX_RANGE"]
+
+
+def test_decode_step_replayed_from_a_cuda_graph_equals_the_eager_step():
+    # append + index + attention captured once into a CUDA graph (the calls allocate nothing given their
+    # buffers and set kernel attributes only on first use); every replay gives the eager step's results
+    dw = workloads.DecodeWorkload("decode_graph", 55, (8, 300, 1037, 2052), topk=32)
+    inp = workloads.decode_inputs(dw)
+    bt = dw.block_table()
+    k8, sk, kv, st = _fill(dw, inp, bt, upto=[L // 4 - 1 if L % 4 == 0 else L // 4 for L in dw.seq_lens])
+    p = _params(dw)
+    comp = [b for b, L in enumerate(dw.seq_lens) if L % 4 == 0]
+    starts = np.concatenate([[0], np.cumsum(dw.seq_lens)])[:-1]
+    t = lambda a: torch.tensor(a, dtype=torch.int32, device="cuda")
+    k_all = torch.cat(inp.k).cuda()
+    g_all = torch.from_numpy(np.concatenate(inp.gate)).cuda()
+    ape = torch.from_numpy(inp.ape).cuda()
+    a_tok = t([int(starts[b]) + dw.seq_lens[b] - 4 for b in comp])
+    a_seq, a_idx = t(comp), t([dw.seq_lens[b] // 4 - 1 for b in comp])
+    btd = torch.from_numpy(bt).cuda()
+    lens = t(list(dw.seq_lens))
+    q_idx, w, q_lat = inp.q_idx.cuda(), torch.from_numpy(inp.w).cuda(), inp.q_lat.cuda()
+    ws = torch.empty(K.decode_workspace_bytes(p, dw.B, dw.max_pages), dtype=torch.uint8, device="cuda")
+    rows = torch.empty((dw.B, dw.W), dtype=torch.int32, device="cuda")
+    out = torch.empty_like(q_lat)
+    lse = torch.empty((dw.B, dw.n_heads), dtype=torch.float32, device="cuda")
+
+    def step():
+        K.paged_append(k_all, g_all, ape, a_tok, a_seq, a_idx, btd, dw.n_pages, p, k8, sk, status=st)
+        K.decode_index(q_idx, w, k8, sk, btd, lens, dw.topk, p, dw.W, workspace=ws, indices=rows, status=st)
+        K.sparse_mla_fwd_rows(q_lat, kv, rows, dw.scale, out=out, lse=lse, status=st)
+
+    step()                                            # eager (also the first use of every kernel)
+    torch.cuda.synchronize()
+    assert K.check_status(st) == 0
+    ref = (k8.clone(), sk.clone(), rows.clone(), out.clone(), lse.clone())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step()
+    for _ in range(3):
+        rows.fill_(-7)
+        out.zero_()
+        lse.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert K.check_status(st) == 0
+        for a, b in zip((k8, sk, rows, out, lse), ref):
+            assert torch.equal(a, b)
