@@ -79,7 +79,8 @@ MLA_TRAFFIC_PER_TOKEN = {"mla-tc5": 537.2e6 / 4096, "mla-tc6": (309.190144e6 + 2
                          "mla-tc7": (308.482304e6 + 227.556096e6) / 4096,
                          "mla-tc8": (308.578304e6 + 228.362496e6) / 4096,
                          "mla-tc9": (308.474880e6 + 227.327232e6) / 4096,
-                         "mla-tc11": (308.508416e6 + 228.636416e6) / 4096}
+                         "mla-tc11": (308.508416e6 + 228.636416e6) / 4096,
+                         "mla-tc12": (309.426688e6 + 227.824128e6) / 4096}
 # DRAM bytes of one scoring launch (ncu dram__bytes_read.sum + dram__bytes_write.sum), captured at the
 # bench's own single-document T=32768 workload; tied to the kernel generation and used only for that T.
 SCORE_TRAFFIC_T32768 = {"score-tc2": 130.948352e6 + 474.102272e6, "score-tc3": 130.935808e6 + 473.886208e6}

@@ -534,6 +534,6 @@ const char* kpool_strerror(int code) {
 
 // The tags after the arch name identify the kernel generations (used to match
 // stored profiler counters to the code that produced them).
-const char* kpool_version(void) { return "kpooldsa 0.17 sm_103a mla-tc11 score-tc3 select5 proj1 bwd4 decode2 pool2 hadamard3"; }
+const char* kpool_version(void) { return "kpooldsa 0.18 sm_103a mla-tc12 score-tc3 select5 proj1 bwd4 decode2 pool2 hadamard3"; }
 
 }  // extern "C"

@@ -237,6 +237,19 @@ __global__ void __launch_bounds__(THREADS, 1) sparse_mla_tc_kernel(const uint16_
     const uint32_t s_base = tc::smem_u32(smem);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     volatile int* abort_flag = &sm.abort;
+    // The first query's Q and the index rows of the first two queries into L2 before anything else (the
+    // in-loop prefetches run ahead of later queries only).  With one query per CTA (a decode step) nothing
+    // else hides their HBM latency: the row scan waits on the row and the Q store on 16 scattered loads per
+    // producer lane.
+    if (tid == 32 * 11) {
+        const int i0 = blockIdx.x;
+        tc::prefetch_l2(q_lat + (int64_t)i0 * H * D_LAT, (uint32_t)(H * D_LAT * 2));
+        if ((W & 3) == 0 && (reinterpret_cast<uintptr_t>(indices) & 15u) == 0) {
+            tc::prefetch_l2(indices + (int64_t)i0 * W, (uint32_t)W * 4u);
+            if (i0 + (int)gridDim.x < n_rows)
+                tc::prefetch_l2(indices + (int64_t)(i0 + (int)gridDim.x) * W, (uint32_t)W * 4u);
+        }
+    }
 
     if (tid == 0) {
         tc::mbar_init(tc::smem_u32(&sm.q_full), NGATH);   // each producer warp: its Q columns stored (+ nb)
