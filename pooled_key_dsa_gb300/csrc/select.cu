@@ -7,15 +7,19 @@
 //
 // A 256-thread block ranks one query row at a time.  Scores become order-preserving uint32
 // keys.  Rows of up to 8192 candidate pools (every row of a document of up to
-// 32768 tokens) take the register path: each thread holds 32 keys (pools
-// t, t+256, ...; loads coalesced), a three-level radix select (bits 31..21,
-// 20..10, 9..0) over the registers finds the key K of the topk-th best pool
-// and how many pools equal to K still fit, and the ordered compaction ranks
-// the kept pools with one ballot per 256-pool column and one block scan over
-// the (column, warp) counts.  The kept pools are those with key > K plus the
-// first pools with key == K that still fit (lower pool index wins ties); their
-// positions are written in pool order, so the row comes out ascending without
-// a sort.
+// 32768 tokens) are ranked from registers on the contiguous path: the row is
+// copied into shared memory so that thread t then holds 2-8 consecutive 16-byte
+// units (4 pools each, as many as the row length needs) with conflict-free
+// loads.  A three-level radix select (bits 31..21, 20..10, 9..0) over the
+// registers finds the key K of the topk-th best pool and how many pools equal
+// to K still fit; a level whose bin holds exactly the keys still needed is
+// kept whole and ends the search.  The kept pools are those with key > K plus
+// the first pools with key == K that still fit (lower pool index wins ties).
+// One block scan of each thread's count of kept pools gives every thread the
+// rank of its first one, and each thread writes its pools' positions in pool
+// order, so the row comes out ascending without a sort.  The few rows whose
+// copy would not fit the buffer keep the register path (32 keys per thread,
+// pools t, t+256, ..., ranked with one ballot per 256-pool column).
 //
 // Longer rows (documents of more than 32768 tokens) are ranked in chunks of
 // 8192 pools: the same levels, and the same compaction chunk by chunk,
